@@ -1,1 +1,244 @@
-"""Fine-grained FP8 quantisation and block-scaled FP8 GEMM for GB300 (sm_103a)."""
+"""Fine-grained FP8 quantisation and block-scaled FP8 GEMM for GB300 (sm_103a).
+
+Thin ctypes binding over ``libfp8fg.so`` (C ABI declared in
+``include/fp8fg.h``). This module only marshals arguments: it takes torch
+tensors that live on the GPU, allocates outputs with torch, and passes raw
+device pointers, sizes and the current CUDA stream to the library. Every step
+of the computation runs in the library's CUDA kernels; there is no fallback.
+If the library is missing or fails to load, every call raises.
+
+Entry points (same names as the C ABI):
+    fp8_quant_1x128(x, transpose=False)     -> (q, scales)
+    fp8_quant_128x128(w)                    -> (q, scales)
+    fp8_gemm_blockscaled(mode, a, sa, b, sb, out_dtype) -> C
+    fp8_grouped_gemm(xq, sx, row_index, expert_offsets, wq, sw, n_rows, out_dtype) -> Y
+plus the convenience wrappers fprop / dgrad / wgrad and device_status().
+"""
+import ctypes
+import os
+
+FPROP, DGRAD, WGRAD = 0, 1, 2
+OUT_F32, OUT_BF16 = 0, 1
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libfp8fg.so")
+_lib = None
+
+
+class Fp8fgError(RuntimeError):
+    def __init__(self, code, what):
+        self.code = code
+        super().__init__("%s: %s (status %d)" % (what, status_str(code) if _lib else "?", code))
+
+
+def lib():
+    """Load libfp8fg.so (raises if it has not been built)."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(LIB_PATH):
+            raise RuntimeError(
+                "libfp8fg.so is not built; run `python fp8_fine_grained_gb300/build.py` "
+                "(or __graft_entry__.build()) first")
+        L = ctypes.CDLL(LIB_PATH)
+        P, I64, I32 = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int
+        L.fp8_quant_1x128.argtypes = [P, I64, I64, I64, P, I64, P, I64, I32, P]
+        L.fp8_quant_128x128.argtypes = [P, I64, I64, I64, P, I64, P, P]
+        L.fp8_gemm_blockscaled.argtypes = [I32, P, P, I64, I64, P, P, I64, I64, I64, I64, I64, P, I32, I64, P]
+        L.fp8_grouped_gemm.argtypes = [P, P, I64, I64, P, P, ctypes.c_int32, I64, P, P, I64, I64, P, I32, I64, P]
+        L.fp8fg_status_str.argtypes = [I32]
+        L.fp8fg_status_str.restype = ctypes.c_char_p
+        L.fp8fg_device_status.argtypes = [P]
+        L.fp8fg_version.argtypes = []
+        L.fp8fg_test_skip_first_load.argtypes = [I32]
+        L.fp8fg_set_wait_limit_ns.argtypes = [I64]
+        for f in ("fp8_quant_1x128", "fp8_quant_128x128", "fp8_gemm_blockscaled", "fp8_grouped_gemm",
+                  "fp8fg_device_status", "fp8fg_version", "fp8fg_test_skip_first_load",
+                  "fp8fg_set_wait_limit_ns"):
+            getattr(L, f).restype = I32
+        _lib = L
+    return _lib
+
+
+def status_str(code):
+    return lib().fp8fg_status_str(int(code)).decode()
+
+
+def _check(rc, what):
+    if rc != 0:
+        raise Fp8fgError(rc, what)
+
+
+def _torch():
+    import torch
+    return torch
+
+
+def _stream(stream):
+    torch = _torch()
+    s = stream if stream is not None else torch.cuda.current_stream()
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+def _ptr(t):
+    return ctypes.c_void_p(t.data_ptr()) if t is not None else None
+
+
+def _rowmajor(t, name):
+    if t.dim() != 2 or t.stride(1) != 1:
+        raise ValueError("%s must be a 2-D row-major tensor (unit inner stride)" % name)
+    if not t.is_cuda:
+        raise ValueError("%s must be a CUDA tensor" % name)
+
+
+def _pad(n, m):
+    return (n + m - 1) // m * m
+
+
+# ------------------------------------------------------------- quantise ----
+
+def fp8_quant_1x128(x, transpose=False, q=None, scales=None, stream=None):
+    """E4M3 codes and FP32 scales of a bf16 matrix in 1x128 tiles.
+
+    transpose=False: x [rows, cols] grouped per row along cols (cols % 128 == 0);
+        returns q uint8 [rows, cols], scales float32 [cols/128, ld_s>=rows].
+    transpose=True: groups of 128 rows per column, output transposed
+        (rows % 128 == 0); returns q uint8 [cols, rows], scales [rows/128, ld_s>=cols].
+    """
+    torch = _torch()
+    _rowmajor(x, "x")
+    if x.dtype != torch.bfloat16:
+        raise ValueError("x must be bfloat16")
+    rows, cols = x.shape
+    if not transpose:
+        if q is None:
+            q = torch.empty((rows, cols), dtype=torch.uint8, device=x.device)
+        if scales is None:
+            scales = torch.empty((cols // 128, _pad(max(rows, 1), 4)), dtype=torch.float32, device=x.device)
+    else:
+        if q is None:
+            q = torch.empty((cols, rows), dtype=torch.uint8, device=x.device)
+        if scales is None:
+            scales = torch.empty((rows // 128, _pad(max(cols, 1), 4)), dtype=torch.float32, device=x.device)
+    rc = lib().fp8_quant_1x128(_ptr(x), rows, cols, x.stride(0), _ptr(q), q.stride(0), _ptr(scales),
+                               scales.stride(0), 1 if transpose else 0, _stream(stream))
+    _check(rc, "fp8_quant_1x128")
+    return q, scales
+
+
+def fp8_quant_128x128(w, q=None, scales=None, stream=None):
+    """E4M3 codes and FP32 scales of a bf16 weight [N, K] in 128x128 blocks.
+    A 3-D weight [E, N, K] (MoE experts) is quantised as [E*N, K]."""
+    torch = _torch()
+    shape = w.shape
+    w2 = w.reshape(-1, shape[-1]) if w.dim() == 3 else w
+    _rowmajor(w2, "w")
+    if w.dtype != torch.bfloat16:
+        raise ValueError("w must be bfloat16")
+    N, K = w2.shape
+    if q is None:
+        q = torch.empty(shape, dtype=torch.uint8, device=w.device)
+    if scales is None:
+        scales = torch.empty(tuple(shape[:-2]) + (shape[-2] // 128, K // 128), dtype=torch.float32,
+                             device=w.device)
+    q2 = q.reshape(-1, K)
+    rc = lib().fp8_quant_128x128(_ptr(w2), N, K, w2.stride(0), _ptr(q2), q2.stride(0), _ptr(scales),
+                                 _stream(stream))
+    _check(rc, "fp8_quant_128x128")
+    return q, scales
+
+
+# ----------------------------------------------------------------- GEMM ----
+
+def _out_code(dtype):
+    torch = _torch()
+    if dtype == torch.bfloat16:
+        return OUT_BF16
+    if dtype == torch.float32:
+        return OUT_F32
+    raise ValueError("output dtype must be bfloat16 or float32")
+
+
+def fp8_gemm_blockscaled(mode, a, sa, b, sb, out_dtype=None, c=None, stream=None):
+    """Block-scaled FP8 GEMM (see include/fp8fg.h for the three modes).
+
+    FPROP: a [M,K] 1x128 + sa [K/128, >=M]; b [N,K] 128x128 + sb [N/128, K/128] -> C [M,N]
+    DGRAD: a [M,K] 1x128 + sa [K/128, >=M]; b [K,N] 128x128 + sb [K/128, N/128] -> C [M,N]
+    WGRAD: a [M,K] + sa [K/128, >=M]; b [N,K] + sb [K/128, >=N] (both grouped along K) -> C [M,N]
+    """
+    torch = _torch()
+    for t, n in ((a, "a"), (b, "b"), (sa, "sa"), (sb, "sb")):
+        _rowmajor(t, n)
+    M, K = a.shape
+    N = b.shape[1] if mode == DGRAD else b.shape[0]
+    if out_dtype is None:
+        out_dtype = torch.float32 if mode == WGRAD else torch.bfloat16
+    if c is None:
+        c = torch.empty((M, N), dtype=out_dtype, device=a.device)
+    _rowmajor(c, "c")
+    rc = lib().fp8_gemm_blockscaled(mode, _ptr(a), _ptr(sa), a.stride(0), sa.stride(0), _ptr(b), _ptr(sb),
+                                    b.stride(0), sb.stride(0), M, N, K, _ptr(c), _out_code(c.dtype),
+                                    c.stride(0), _stream(stream))
+    _check(rc, "fp8_gemm_blockscaled")
+    return c
+
+
+def fprop(xq, sx, wq, sw, out_dtype=None, c=None, stream=None):
+    """Y = X W^T from fp8_quant_1x128(X) and fp8_quant_128x128(W)."""
+    return fp8_gemm_blockscaled(FPROP, xq, sx, wq, sw, out_dtype, c, stream)
+
+
+def dgrad(dyq, sdy, wq, sw, out_dtype=None, c=None, stream=None):
+    """dX = dY W from fp8_quant_1x128(dY) and the forward weight's fp8_quant_128x128."""
+    return fp8_gemm_blockscaled(DGRAD, dyq, sdy, wq, sw, out_dtype, c, stream)
+
+
+def wgrad(dyqT, sdyT, xqT, sxT, out_dtype=None, c=None, stream=None):
+    """dW = dY^T X from fp8_quant_1x128(dY, transpose=True) and fp8_quant_1x128(X, transpose=True)."""
+    return fp8_gemm_blockscaled(WGRAD, dyqT, sdyT, xqT, sxT, out_dtype, c, stream)
+
+
+def fp8_grouped_gemm(xq, sx, row_index, expert_offsets, wq, sw, n_rows, out_dtype=None, y=None, stream=None):
+    """MoE expert GEMM: Y[r] = fprop(Xq[row_index[r]], Wq[e]) for r in expert e's range.
+
+    xq [T, K] uint8, sx [K/128, >=T]; row_index int32 [n_rows]; expert_offsets
+    int32 [E+1]; wq uint8 [E, N, K]; sw float32 [E, N/128, K/128].
+    """
+    torch = _torch()
+    _rowmajor(xq, "xq")
+    _rowmajor(sx, "sx")
+    if row_index.dtype != torch.int32 or expert_offsets.dtype != torch.int32:
+        raise ValueError("row_index and expert_offsets must be int32")
+    if not (row_index.is_contiguous() and expert_offsets.is_contiguous() and wq.is_contiguous()
+            and sw.is_contiguous()):
+        raise ValueError("row_index, expert_offsets, wq, sw must be contiguous")
+    T, K = xq.shape
+    E, N, K2 = wq.shape
+    if K2 != K or xq.stride(0) != K:
+        raise ValueError("xq must be [T, K] contiguous with the experts' K")
+    if out_dtype is None:
+        out_dtype = torch.bfloat16
+    if y is None:
+        y = torch.empty((n_rows, N), dtype=out_dtype, device=xq.device)
+    _rowmajor(y, "y")
+    rc = lib().fp8_grouped_gemm(_ptr(xq), _ptr(sx), sx.stride(0), T, _ptr(row_index), _ptr(expert_offsets), E,
+                                n_rows, _ptr(wq), _ptr(sw), N, K, _ptr(y), _out_code(y.dtype), y.stride(0),
+                                _stream(stream))
+    _check(rc, "fp8_grouped_gemm")
+    return y
+
+
+def device_status(stream=None):
+    """Synchronise the stream and return (and clear) the device status word."""
+    return lib().fp8fg_device_status(_stream(stream))
+
+
+def set_wait_limit_ns(ns):
+    _check(lib().fp8fg_set_wait_limit_ns(int(ns)), "fp8fg_set_wait_limit_ns")
+
+
+def inject_skip_first_load(skip=True):
+    _check(lib().fp8fg_test_skip_first_load(1 if skip else 0), "fp8fg_test_skip_first_load")
+
+
+def version():
+    return lib().fp8fg_version()

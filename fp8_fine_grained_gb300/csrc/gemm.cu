@@ -1,0 +1,728 @@
+// Block-scaled FP8 GEMM with promotion every 128 of the contraction
+// dimension, on sm_103a tensor cores (tcgen05), for the forward, data-
+// gradient and weight-gradient products and for MoE experts over a row
+// index.
+//
+// Method (innerforce.co.kr, increased-precision accumulation paragraph;
+// yunhecapital.com 2.2.3; tonho.wtf DeepSeek-V3 entry, "como funciona"):
+// the tensor cores form the FP8 x FP8 product of one 128-wide contraction
+// block; that partial sum is then moved off the tensor cores, multiplied by
+// the block's two dequantisation scales and added to an FP32 accumulator.
+//
+// GB300 design (one CTA per SM, persistent over 128x256 output tiles):
+//   warp 0      TMA producer: A tile 128x128 B and B tile 256x128 B per
+//               contraction block into a 4-stage shared-memory ring
+//               (128-byte swizzle), signalled on mbarriers.
+//   warp 1      MMA issuer: allocates all 512 tensor-memory columns, issues
+//               4 x tcgen05.mma (M128 N256 K32, E4M3 -> FP32) per block into
+//               one of two 256-column TMEM partial buffers, and commits to
+//               the stage's "empty" and the buffer's "full" barrier.
+//   warps 2..9  promotion/epilogue: each thread owns one output row and 128
+//               columns; per block it loads the partial from TMEM
+//               (tcgen05.ld 32x32b), does acc = fma(P, sA*sB, acc) in FP32
+//               registers and frees the TMEM buffer, so the MMA of block
+//               kb+1 overlaps the promotion of block kb. After the last
+//               block it rounds and stores the row.
+// Every wait is bounded (global timer); a wait that runs out records
+// FP8FG_ETIMEOUT in the device status word and all roles leave their loops,
+// drain their own in-flight copies and MMAs, and release tensor memory.
+#include <cuda_bf16.h>
+
+#include "host_common.h"
+#include "ptx.cuh"
+
+namespace fp8fg {
+namespace {
+
+constexpr int BM = 128;        // output rows per tile (TMEM lanes)
+constexpr int BN = 256;        // output columns per tile
+constexpr int BK = 128;        // contraction block = promotion interval = scale group
+constexpr int STAGES = 4;
+constexpr int EPI_WARPS = 8;
+constexpr int NUM_THREADS = (2 + EPI_WARPS) * 32;
+constexpr uint32_t A_STAGE_BYTES = BM * BK;   // 16 KB
+constexpr uint32_t B_STAGE_BYTES = BN * BK;   // 32 KB
+constexpr uint32_t TMEM_COLS = 512;           // two 256-column partial buffers
+constexpr int MAX_EXPERTS = 4096;
+constexpr int MMA_K = 32;                     // K per tcgen05.mma for 8-bit operands
+
+enum Mode { FPROP = 0, DGRAD = 1, WGRAD = 2, GROUPED = 3 };
+
+struct Params {
+    int64_t M, N, K;
+    const float *sA;
+    int64_t ld_sA;
+    const float *sB;
+    int64_t ld_sB;
+    void *C;
+    int64_t ldc;
+    int64_t num_m_tiles, num_n_tiles;
+    int *status;
+    uint64_t wait_limit_ns;
+    int skip_first_load;
+    // grouped mode
+    const int32_t *row_index;
+    const int32_t *expert_offsets;
+    int n_experts;
+    int64_t n_rows;
+    int64_t n_tokens;
+};
+
+struct SmemLayout {
+    // B stages first: every operand read stays well inside the allocation
+    static constexpr uint32_t b_off = 0;
+    static constexpr uint32_t a_off = b_off + STAGES * B_STAGE_BYTES;
+    static constexpr uint32_t bar_off = a_off + STAGES * A_STAGE_BYTES;
+    static constexpr uint32_t full_off = bar_off;
+    static constexpr uint32_t empty_off = full_off + 8 * STAGES;
+    static constexpr uint32_t tfull_off = empty_off + 8 * STAGES;
+    static constexpr uint32_t tempty_off = tfull_off + 8 * 2;
+    static constexpr uint32_t tmem_ptr_off = tempty_off + 8 * 2;
+    static constexpr uint32_t abort_off = tmem_ptr_off + 4;
+    static constexpr uint32_t misc_end = abort_off + 4;
+    static constexpr uint32_t wscale_off = (misc_end + 15) & ~15u;       // WGRAD column scales
+    static constexpr uint32_t wscale_end = wscale_off + EPI_WARPS * 128 * 4;
+    static constexpr uint32_t prefix_off = wscale_end;                    // GROUPED tile prefix
+    static constexpr uint32_t prefix_end = prefix_off + 4 * (MAX_EXPERTS + 1);
+    static constexpr uint32_t total = prefix_end + 1024;                 // + alignment slack
+};
+static_assert(SmemLayout::total <= 232448, "shared memory budget");
+
+struct Tile {
+    int64_t m0;       // first A row (dense) / first output row (grouped)
+    int64_t row_end;  // one past the last valid output row of the tile's group
+    int64_t n0;       // first output column
+    int expert;
+};
+
+__device__ __forceinline__ int64_t grouped_total_tiles(const int32_t *prefix, int n_experts)
+{
+    return prefix[n_experts];
+}
+
+template <int MODE>
+__device__ __forceinline__ Tile decode_tile(int64_t t, const Params &p, const int32_t *prefix)
+{
+    Tile tl;
+    if constexpr (MODE == GROUPED) {
+        // experts are laid out in the tile space one after the other; within
+        // an expert the m-tiles vary fastest, so CTAs running together share
+        // the expert's weight tiles in L2.
+        int lo = 0, hi = p.n_experts;  // find last e with prefix[e] <= t
+        while (hi - lo > 1) {
+            int mid = (lo + hi) >> 1;
+            if (prefix[mid] <= t)
+                lo = mid;
+            else
+                hi = mid;
+        }
+        const int e = lo;
+        const int64_t local = t - prefix[e];
+        int64_t r0 = p.expert_offsets[e], r1 = p.expert_offsets[e + 1];
+        r0 = r0 < 0 ? 0 : (r0 > p.n_rows ? p.n_rows : r0);
+        r1 = r1 > p.n_rows ? p.n_rows : r1;
+        const int64_t mt = (r1 - r0 + BM - 1) / BM;
+        tl.expert = e;
+        tl.m0 = r0 + (local % mt) * BM;
+        tl.row_end = r1;
+        tl.n0 = (local / mt) * BN;
+    } else {
+        // bands of 16 m-tiles, m fastest inside a band: CTAs running at the
+        // same time read ~16 A tiles and ~10 B tiles, all L2-resident.
+        constexpr int64_t BAND = 16;
+        const int64_t per_band = BAND * p.num_n_tiles;
+        const int64_t band = t / per_band, r = t % per_band;
+        const int64_t mfirst = band * BAND;
+        const int64_t gm = (p.num_m_tiles - mfirst) < BAND ? (p.num_m_tiles - mfirst) : BAND;
+        tl.m0 = (mfirst + r % gm) * BM;
+        tl.n0 = (r / gm) * BN;
+        tl.row_end = p.M;
+        tl.expert = 0;
+    }
+    return tl;
+}
+
+// Block-wide exclusive prefix over experts of (m-tiles x n-tiles); flags
+// malformed offsets. Runs once per CTA at kernel start.
+__device__ void build_group_prefix(const Params &p, int32_t *prefix)
+{
+    __shared__ int32_t warp_sums[NUM_THREADS / 32];
+    const int E = p.n_experts;
+    const int per = (E + NUM_THREADS - 1) / NUM_THREADS;
+    const int e0 = threadIdx.x * per;
+    int32_t local[16];  // per <= 4096/320 + 1 = 13
+    int32_t sum = 0;
+    for (int i = 0; i < per && i < 16; ++i) {
+        const int e = e0 + i;
+        int32_t v = 0;
+        if (e < E) {
+            int64_t r0 = p.expert_offsets[e], r1 = p.expert_offsets[e + 1];
+            if (r0 < 0 || r1 < r0 || r1 > p.n_rows)
+                atomicCAS(p.status, 0, FP8FG_EDEVICE);
+            r0 = r0 < 0 ? 0 : (r0 > p.n_rows ? p.n_rows : r0);
+            r1 = r1 > p.n_rows ? p.n_rows : r1;
+            const int64_t m = r1 > r0 ? r1 - r0 : 0;
+            v = (int32_t)(((m + BM - 1) / BM) * p.num_n_tiles);
+        }
+        local[i] = v;
+        sum += v;
+    }
+    // inclusive scan of per-thread sums
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    int32_t x = sum;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        int32_t y = __shfl_up_sync(0xffffffffu, x, o);
+        if (lane >= o)
+            x += y;
+    }
+    if (lane == 31)
+        warp_sums[warp] = x;
+    __syncthreads();
+    int32_t base = 0;
+    for (int w = 0; w < warp; ++w)
+        base += warp_sums[w];
+    int32_t run = base + x - sum;  // exclusive prefix of this thread
+    for (int i = 0; i < per && i < 16; ++i) {
+        const int e = e0 + i;
+        if (e < E)
+            prefix[e] = run;
+        run += local[i];
+    }
+    if (threadIdx.x == NUM_THREADS - 1)
+        prefix[E] = run;  // total (last thread's run ends at the grand total)
+    __syncthreads();
+}
+
+template <int MODE, bool OUT_BF16>
+__global__ void __launch_bounds__(NUM_THREADS, 1)
+    gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB, const Params p)
+{
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    const uint32_t sbase = smem_u32(smem);
+    const uint32_t full_bar = sbase + SmemLayout::full_off;
+    const uint32_t empty_bar = sbase + SmemLayout::empty_off;
+    const uint32_t tfull_bar = sbase + SmemLayout::tfull_off;
+    const uint32_t tempty_bar = sbase + SmemLayout::tempty_off;
+    volatile uint32_t *tmem_ptr = reinterpret_cast<volatile uint32_t *>(smem + SmemLayout::tmem_ptr_off);
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + SmemLayout::abort_off);
+    int32_t *prefix = reinterpret_cast<int32_t *>(smem + SmemLayout::prefix_off);
+
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    const WaitCtl wc{abort_flag, p.status, p.wait_limit_ns};
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < STAGES; ++s) {
+            mbar_init(full_bar + 8 * s, 1);
+            mbar_init(empty_bar + 8 * s, 1);
+        }
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(tfull_bar + 8 * b, 1);
+            mbar_init(tempty_bar + 8 * b, EPI_WARPS);
+        }
+        *abort_flag = 0;
+        fence_mbar_init();
+        tma_prefetch_desc(&tmA);
+        tma_prefetch_desc(&tmB);
+    }
+    if (warp == 1) {
+        tmem_alloc(sbase + SmemLayout::tmem_ptr_off, TMEM_COLS);
+        tmem_relinquish();
+    }
+    if constexpr (MODE == GROUPED)
+        build_group_prefix(p, prefix);
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem_base = *tmem_ptr;
+
+    const int64_t num_tiles =
+        (MODE == GROUPED) ? (int64_t)grouped_total_tiles(prefix, p.n_experts) : p.num_m_tiles * p.num_n_tiles;
+    const int num_kb = (int)(p.K / BK);
+
+    if (warp == 0) {
+        // ------------------------------------------------------ producer ----
+        uint32_t stage = 0, phase = 0;
+        uint32_t filled_mask = 0, fill_parity = 0;  // per stage: a fill was issued, and its parity
+        bool skip = p.skip_first_load && blockIdx.x == 0;
+        bool ok = true;
+        for (int64_t t = blockIdx.x; t < num_tiles && ok; t += gridDim.x) {
+            const Tile tl = decode_tile<MODE>(t, p, prefix);
+            int32_t tok[4] = {0, 0, 0, 0};
+            if constexpr (MODE == GROUPED) {
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                    const int64_t r = tl.m0 + lane * 4 + i;
+                    int32_t v = p.row_index[r < tl.row_end ? r : tl.m0];
+                    if (v < 0 || v >= p.n_tokens) {
+                        atomicCAS(p.status, 0, FP8FG_EDEVICE);
+                        v = 0;
+                    }
+                    tok[i] = v;
+                }
+            }
+            for (int kb = 0; kb < num_kb; ++kb) {
+                bool got = true;
+                if (lane == 0)
+                    got = mbar_wait(empty_bar + 8 * stage, phase ^ 1, wc, FP8FG_ETIMEOUT);
+                got = __shfl_sync(0xffffffffu, got ? 1 : 0, 0) != 0;
+                if (!got) {
+                    ok = false;
+                    break;
+                }
+                const uint32_t fb = full_bar + 8 * stage;
+                const uint32_t a_dst = sbase + SmemLayout::a_off + stage * A_STAGE_BYTES;
+                const uint32_t b_dst = sbase + SmemLayout::b_off + stage * B_STAGE_BYTES;
+                if (skip) {
+                    skip = false;  // withhold this load: consumers must time out
+                } else {
+                    uint32_t bytes = A_STAGE_BYTES + B_STAGE_BYTES;
+                    bool second_half = true;
+                    if constexpr (MODE == DGRAD) {
+                        second_half = tl.n0 + 128 < p.N;
+                        if (!second_half)
+                            bytes = A_STAGE_BYTES + B_STAGE_BYTES / 2;
+                    }
+                    if (lane == 0) {
+                        mbar_arrive_expect_tx(fb, bytes);
+                        filled_mask |= 1u << stage;
+                        fill_parity = (fill_parity & ~(1u << stage)) | (phase << stage);
+                    }
+                    __syncwarp();
+                    if constexpr (MODE == GROUPED) {
+                        tma_gather4(a_dst + lane * 512, &tmA, kb * BK, tok[0], tok[1], tok[2], tok[3], fb);
+                        if (lane == 0)
+                            tma_load_2d(b_dst, &tmB, kb * BK, (int32_t)(tl.expert * p.N + tl.n0), fb);
+                    } else if (lane == 0) {
+                        tma_load_2d(a_dst, &tmA, kb * BK, (int32_t)tl.m0, fb);
+                        if constexpr (MODE == DGRAD) {
+                            // B is the weight [K][N] read N-contiguous: two
+                            // 128(K) x 128(N) boxes, one per 128-column half.
+                            tma_load_2d(b_dst, &tmB, (int32_t)tl.n0, kb * BK, fb);
+                            if (second_half)
+                                tma_load_2d(b_dst + B_STAGE_BYTES / 2, &tmB, (int32_t)tl.n0 + 128, kb * BK, fb);
+                        } else {
+                            tma_load_2d(b_dst, &tmB, kb * BK, (int32_t)tl.n0, fb);
+                        }
+                    }
+                }
+                if (++stage == STAGES) {
+                    stage = 0;
+                    phase ^= 1;
+                }
+            }
+        }
+        if (!ok && lane == 0) {
+            // drain: every issued fill must land before the CTA exits
+            WaitCtl drain{abort_flag, p.status, p.wait_limit_ns};
+            for (int s = 0; s < STAGES; ++s) {
+                if (!(filled_mask & (1u << s)))
+                    continue;
+                const uint32_t bar = full_bar + 8 * s, par = (fill_parity >> s) & 1u;
+                const uint64_t t0 = global_timer_ns();
+                while (!mbar_try_wait(bar, par) && global_timer_ns() - t0 < drain.limit_ns) {
+                }
+            }
+        }
+    } else if (warp == 1) {
+        // ---------------------------------------------------------- MMA ----
+        if (lane == 0) {
+            constexpr uint32_t IDESC = idesc_e4m3_f32(BM, BN, MODE == DGRAD);
+            uint32_t stage = 0, phase = 0, buf = 0, tphase = 0;
+            int committed = 0;
+            uint32_t last_buf = 0, last_par = 0;
+            bool ok = true;
+            for (int64_t t = blockIdx.x; t < num_tiles && ok; t += gridDim.x) {
+                for (int kb = 0; kb < num_kb; ++kb) {
+                    if (!mbar_wait(tempty_bar + 8 * buf, tphase ^ 1, wc, FP8FG_ETIMEOUT)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    if (!mbar_wait(full_bar + 8 * stage, phase, wc, FP8FG_ETIMEOUT)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    const uint32_t a_addr = sbase + SmemLayout::a_off + stage * A_STAGE_BYTES;
+                    const uint32_t b_addr = sbase + SmemLayout::b_off + stage * B_STAGE_BYTES;
+                    const uint32_t d = tmem_base + buf * BN;
+#pragma unroll
+                    for (int k = 0; k < BK / MMA_K; ++k) {
+                        // K-major, 128-byte rows: step K by 32 bytes inside the swizzle atom
+                        const uint64_t adesc = smem_desc_sw128(a_addr + k * MMA_K, 0, 1024);
+                        uint64_t bdesc;
+                        if constexpr (MODE == DGRAD)
+                            // N-major: 32 K-rows = 4 groups of 8 rows (1024 B each);
+                            // the two 128-column halves are 16 KB apart.
+                            bdesc = smem_desc_sw128(b_addr + k * MMA_K * 128, B_STAGE_BYTES / 2, 1024);
+                        else
+                            bdesc = smem_desc_sw128(b_addr + k * MMA_K, 0, 1024);
+                        mma_f8f6f4(d, adesc, bdesc, IDESC, k > 0 ? 1u : 0u);
+                    }
+                    mma_commit(empty_bar + 8 * stage);
+                    mma_commit(tfull_bar + 8 * buf);
+                    committed = 1;
+                    last_buf = buf;
+                    last_par = tphase;
+                    if (++stage == STAGES) {
+                        stage = 0;
+                        phase ^= 1;
+                    }
+                    if (++buf == 2) {
+                        buf = 0;
+                        tphase ^= 1;
+                    }
+                }
+            }
+            if (!ok && committed) {
+                // drain: the last commit covers every MMA issued before it
+                const uint32_t bar = tfull_bar + 8 * last_buf;
+                const uint64_t t0 = global_timer_ns();
+                while (!mbar_try_wait(bar, last_par) && global_timer_ns() - t0 < p.wait_limit_ns) {
+                }
+            }
+        }
+        __syncwarp();
+    } else {
+        // ------------------------------------------ promotion / epilogue ----
+        const int ew = warp - 2;
+        const int quarter = warp & 3;        // TMEM lanes 32*quarter .. +31
+        const int half = ew >> 2;            // output columns half*128 .. +127 of the tile
+        const int row_in_tile = quarter * 32 + lane;
+        float *wscale = reinterpret_cast<float *>(smem + SmemLayout::wscale_off) + ew * 128;
+        uint32_t buf = 0, tphase = 0;
+        bool ok = true;
+        for (int64_t t = blockIdx.x; t < num_tiles && ok; t += gridDim.x) {
+            const Tile tl = decode_tile<MODE>(t, p, prefix);
+            const int64_t row = tl.m0 + row_in_tile;  // A row (dense) / output row (grouped)
+            const bool row_ok = row < tl.row_end;
+            const int64_t col0 = tl.n0 + half * 128;
+            const bool cols_ok = col0 < p.N;
+            int64_t arow = row;  // row of the scale array sA
+            if constexpr (MODE == GROUPED) {
+                int32_t v = row_ok ? p.row_index[row] : 0;
+                arow = (v < 0 || v >= p.n_tokens) ? 0 : v;
+            }
+            auto load_sa = [&](int kb) -> float { return row_ok ? __ldg(p.sA + (int64_t)kb * p.ld_sA + arow) : 0.0f; };
+            auto load_sb = [&](int kb) -> float {
+                if (!cols_ok)
+                    return 0.0f;
+                if constexpr (MODE == FPROP)
+                    return __ldg(p.sB + (col0 / 128) * p.ld_sB + kb);
+                else if constexpr (MODE == DGRAD)
+                    return __ldg(p.sB + (int64_t)kb * p.ld_sB + col0 / 128);
+                else if constexpr (MODE == GROUPED)
+                    return __ldg(p.sB + ((int64_t)tl.expert * (p.N / 128) + col0 / 128) * (p.K / 128) + kb);
+                else
+                    return 0.0f;
+            };
+            auto load_sbv = [&](int kb) -> float4 {
+                if (!cols_ok)
+                    return make_float4(0.f, 0.f, 0.f, 0.f);
+                return __ldg(reinterpret_cast<const float4 *>(p.sB + (int64_t)kb * p.ld_sB + col0) + lane);
+            };
+
+            float acc[128];
+#pragma unroll
+            for (int j = 0; j < 128; ++j)
+                acc[j] = 0.0f;
+            float sa_next = load_sa(0);
+            float sb_next = 0.0f;
+            float4 sbv_next = make_float4(0.f, 0.f, 0.f, 0.f);
+            if constexpr (MODE == WGRAD)
+                sbv_next = load_sbv(0);
+            else
+                sb_next = load_sb(0);
+
+            for (int kb = 0; kb < num_kb; ++kb) {
+                const float sa = sa_next;
+                const float sb = sb_next;
+                const float4 sbv = sbv_next;
+                if (kb + 1 < num_kb) {
+                    sa_next = load_sa(kb + 1);
+                    if constexpr (MODE == WGRAD)
+                        sbv_next = load_sbv(kb + 1);
+                    else
+                        sb_next = load_sb(kb + 1);
+                }
+                if constexpr (MODE == WGRAD) {
+                    reinterpret_cast<float4 *>(wscale)[lane] = sbv;
+                    __syncwarp();
+                }
+                const bool got = mbar_wait(tfull_bar + 8 * buf, tphase, wc, FP8FG_ETIMEOUT);
+                if (!__all_sync(0xffffffffu, got)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                const uint32_t taddr = tmem_base + ((uint32_t)(quarter * 32) << 16) + buf * BN + half * 128;
+                const float s = sa * sb;
+                uint32_t r[2][16];
+                tmem_ld16(taddr, r[0]);
+                tmem_wait_ld_into(r[0]);
+#pragma unroll
+                for (int c = 0; c < 8; ++c) {
+                    if (c + 1 < 8)
+                        tmem_ld16(taddr + (c + 1) * 16, r[(c + 1) & 1]);
+                    if constexpr (MODE == WGRAD) {
+#pragma unroll
+                        for (int j = 0; j < 16; j += 4) {
+                            const float4 sc = reinterpret_cast<const float4 *>(wscale)[(c * 16 + j) >> 2];
+                            acc[c * 16 + j + 0] = fmaf(__uint_as_float(r[c & 1][j + 0]), sa * sc.x, acc[c * 16 + j + 0]);
+                            acc[c * 16 + j + 1] = fmaf(__uint_as_float(r[c & 1][j + 1]), sa * sc.y, acc[c * 16 + j + 1]);
+                            acc[c * 16 + j + 2] = fmaf(__uint_as_float(r[c & 1][j + 2]), sa * sc.z, acc[c * 16 + j + 2]);
+                            acc[c * 16 + j + 3] = fmaf(__uint_as_float(r[c & 1][j + 3]), sa * sc.w, acc[c * 16 + j + 3]);
+                        }
+                    } else {
+#pragma unroll
+                        for (int j = 0; j < 16; ++j)
+                            acc[c * 16 + j] = fmaf(__uint_as_float(r[c & 1][j]), s, acc[c * 16 + j]);
+                    }
+                    if (c + 1 < 8)
+                        tmem_wait_ld_into(r[(c + 1) & 1]);
+                }
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0)
+                    mbar_arrive(tempty_bar + 8 * buf);
+                if (++buf == 2) {
+                    buf = 0;
+                    tphase ^= 1;
+                }
+            }
+            if (!ok)
+                break;
+            if (row_ok && cols_ok) {
+                if constexpr (OUT_BF16) {
+                    uint4 *dst = reinterpret_cast<uint4 *>(static_cast<__nv_bfloat16 *>(p.C) + row * p.ldc + col0);
+#pragma unroll
+                    for (int j = 0; j < 128; j += 8) {
+                        uint4 o;
+                        __nv_bfloat162 h0 = __floats2bfloat162_rn(acc[j + 0], acc[j + 1]);
+                        __nv_bfloat162 h1 = __floats2bfloat162_rn(acc[j + 2], acc[j + 3]);
+                        __nv_bfloat162 h2 = __floats2bfloat162_rn(acc[j + 4], acc[j + 5]);
+                        __nv_bfloat162 h3 = __floats2bfloat162_rn(acc[j + 6], acc[j + 7]);
+                        o.x = *reinterpret_cast<uint32_t *>(&h0);
+                        o.y = *reinterpret_cast<uint32_t *>(&h1);
+                        o.z = *reinterpret_cast<uint32_t *>(&h2);
+                        o.w = *reinterpret_cast<uint32_t *>(&h3);
+                        dst[j / 8] = o;
+                    }
+                } else {
+                    float4 *dst = reinterpret_cast<float4 *>(static_cast<float *>(p.C) + row * p.ldc + col0);
+#pragma unroll
+                    for (int j = 0; j < 128; j += 4)
+                        dst[j / 4] = make_float4(acc[j], acc[j + 1], acc[j + 2], acc[j + 3]);
+                }
+            }
+        }
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        tc_fence_after();
+        tmem_dealloc(tmem_base, TMEM_COLS);
+    }
+}
+
+// ------------------------------------------------------------ host side ----
+
+using EncodeTiledFn = CUresult (*)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *, const cuuint64_t *,
+                                   const cuuint64_t *, const cuuint32_t *, const cuuint32_t *, CUtensorMapInterleave,
+                                   CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn()
+{
+    static EncodeTiledFn fn = []() -> EncodeTiledFn {
+        void *f = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &q) !=
+                cudaSuccess ||
+            q != cudaDriverEntryPointSuccess) {
+            cudaGetLastError();
+            return nullptr;
+        }
+        return reinterpret_cast<EncodeTiledFn>(f);
+    }();
+    return fn;
+}
+
+// 2-D uint8 tensor [rows][cols] with row pitch `ld` bytes; box
+// box_cols x box_rows, 128-byte swizzle.
+bool make_map(CUtensorMap *m, const void *base, uint64_t cols, uint64_t rows, uint64_t ld, uint32_t box_cols,
+              uint32_t box_rows)
+{
+    EncodeTiledFn fn = encode_fn();
+    if (!fn)
+        return false;
+    cuuint64_t dims[2] = {cols, rows};
+    cuuint64_t strides[1] = {ld};
+    cuuint32_t box[2] = {box_cols, box_rows};
+    cuuint32_t estr[2] = {1, 1};
+    return fn(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void *>(base), dims, strides, box, estr,
+              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+template <int MODE, bool BF16>
+int launch(const CUtensorMap &ta, const CUtensorMap &tb, const Params &p, int grid, cudaStream_t s)
+{
+    auto k = gemm_kernel<MODE, BF16>;
+    if (cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)SmemLayout::total) !=
+        cudaSuccess) {
+        cudaGetLastError();
+        return FP8FG_ECUDA;
+    }
+    k<<<grid, NUM_THREADS, SmemLayout::total, s>>>(ta, tb, p);
+    return launch_status();
+}
+
+template <int MODE>
+int launch_out(int out, const CUtensorMap &ta, const CUtensorMap &tb, const Params &p, int grid, cudaStream_t s)
+{
+    return out == FP8FG_OUT_BF16 ? launch<MODE, true>(ta, tb, p, grid, s) : launch<MODE, false>(ta, tb, p, grid, s);
+}
+
+bool fill_runtime(Params &p)
+{
+    p.status = status_word_ptr();
+    p.wait_limit_ns = wait_limit_ns();
+    p.skip_first_load = take_skip_first_load() ? 1 : 0;
+    return p.status != nullptr;
+}
+
+}  // namespace
+}  // namespace fp8fg
+
+using namespace fp8fg;
+
+extern "C" int fp8_gemm_blockscaled(int mode, const uint8_t *A, const float *sA, int64_t lda, int64_t ld_sA,
+                                    const uint8_t *B, const float *sB, int64_t ldb, int64_t ld_sB, int64_t M,
+                                    int64_t N, int64_t K, void *C, int out, int64_t ldc, void *stream)
+{
+    if (mode < FPROP || mode > WGRAD || (out != FP8FG_OUT_F32 && out != FP8FG_OUT_BF16))
+        return FP8FG_EINVAL;
+    if (M < 0 || N < 0 || K < BK || N % 128 != 0 || K % BK != 0)
+        return FP8FG_EINVAL;
+    if (M >= (1ll << 31) || N >= (1ll << 31) || K >= (1ll << 31))
+        return FP8FG_EINVAL;
+    const int64_t esz = out == FP8FG_OUT_BF16 ? 2 : 4;
+    if (lda < K || ldc < N || ld_sA < M)
+        return FP8FG_EINVAL;
+    if (mode == DGRAD ? (ldb < N || ld_sB < N / 128) : (ldb < K))
+        return FP8FG_EINVAL;
+    if (mode == FPROP && ld_sB < K / 128)
+        return FP8FG_EINVAL;
+    if (mode == WGRAD && ld_sB < N)
+        return FP8FG_EINVAL;
+    if (M == 0 || N == 0)
+        return FP8FG_OK;
+    if (!A || !sA || !B || !sB || !C)
+        return FP8FG_EINVAL;
+    if (!aligned16(A) || !aligned16(B) || !aligned16(C) || !aligned16(sA) || !aligned16(sB) || lda % 16 != 0 ||
+        ldb % 16 != 0 || (ldc * esz) % 16 != 0 || ld_sA % 4 != 0 || (mode == WGRAD && ld_sB % 4 != 0))
+        return FP8FG_EALIGN;
+    if (!device_supported())
+        return FP8FG_EUNSUPPORTED;
+
+    Params p{};
+    p.M = M;
+    p.N = N;
+    p.K = K;
+    p.sA = sA;
+    p.ld_sA = ld_sA;
+    p.sB = sB;
+    p.ld_sB = ld_sB;
+    p.C = C;
+    p.ldc = ldc;
+    p.num_m_tiles = (M + BM - 1) / BM;
+    p.num_n_tiles = (N + BN - 1) / BN;
+    if (!fill_runtime(p))
+        return FP8FG_ECUDA;
+
+    CUtensorMap ta, tb;
+    if (!make_map(&ta, A, (uint64_t)K, (uint64_t)M, (uint64_t)lda, BK, BM))
+        return FP8FG_ECUDA;
+    bool okb;
+    if (mode == DGRAD)  // weight [K][N], N contiguous: boxes of 128 N x 128 K
+        okb = make_map(&tb, B, (uint64_t)N, (uint64_t)K, (uint64_t)ldb, 128, BK);
+    else
+        okb = make_map(&tb, B, (uint64_t)K, (uint64_t)N, (uint64_t)ldb, BK, BN);
+    if (!okb)
+        return FP8FG_ECUDA;
+
+    const int64_t tiles = p.num_m_tiles * p.num_n_tiles;
+    const int sms = sm_count();
+    const int grid = (int)(tiles < sms ? tiles : sms);
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    switch (mode) {
+    case FPROP: return launch_out<FPROP>(out, ta, tb, p, grid, s);
+    case DGRAD: return launch_out<DGRAD>(out, ta, tb, p, grid, s);
+    default: return launch_out<WGRAD>(out, ta, tb, p, grid, s);
+    }
+}
+
+extern "C" int fp8_grouped_gemm(const uint8_t *Xq, const float *sX, int64_t ld_sX, int64_t n_tokens,
+                                const int32_t *row_index, const int32_t *expert_offsets, int32_t n_experts,
+                                int64_t n_rows, const uint8_t *Wq, const float *sW, int64_t N, int64_t K, void *Y,
+                                int out, int64_t ldy, void *stream)
+{
+    if (out != FP8FG_OUT_F32 && out != FP8FG_OUT_BF16)
+        return FP8FG_EINVAL;
+    if (n_tokens < 0 || n_rows < 0 || N < 0 || K < BK || N % 128 != 0 || K % BK != 0)
+        return FP8FG_EINVAL;
+    if (n_experts < 1 || n_experts > MAX_EXPERTS)
+        return FP8FG_EINVAL;
+    if (n_tokens >= (1ll << 31) || n_rows >= (1ll << 31) || K >= (1ll << 31) ||
+        (int64_t)n_experts * N >= (1ll << 31))
+        return FP8FG_EINVAL;
+    const int64_t esz = out == FP8FG_OUT_BF16 ? 2 : 4;
+    if (ld_sX < n_tokens || ldy < N)
+        return FP8FG_EINVAL;
+    if (!expert_offsets)
+        return FP8FG_EINVAL;
+    if (n_rows == 0 || N == 0 || n_tokens == 0) {
+        // nothing can be written; offsets are not inspected
+        return FP8FG_OK;
+    }
+    if (!Xq || !sX || !row_index || !Wq || !sW || !Y)
+        return FP8FG_EINVAL;
+    if (!aligned16(Xq) || !aligned16(Wq) || !aligned16(sX) || !aligned16(Y) || K % 16 != 0 || ld_sX % 4 != 0 ||
+        (ldy * esz) % 16 != 0)
+        return FP8FG_EALIGN;
+    if (!device_supported())
+        return FP8FG_EUNSUPPORTED;
+
+    Params p{};
+    p.M = n_rows;
+    p.N = N;
+    p.K = K;
+    p.sA = sX;
+    p.ld_sA = ld_sX;
+    p.sB = sW;
+    p.ld_sB = K / 128;
+    p.C = Y;
+    p.ldc = ldy;
+    p.num_m_tiles = 0;
+    p.num_n_tiles = (N + BN - 1) / BN;
+    p.row_index = row_index;
+    p.expert_offsets = expert_offsets;
+    p.n_experts = n_experts;
+    p.n_rows = n_rows;
+    p.n_tokens = n_tokens;
+    if (!fill_runtime(p))
+        return FP8FG_ECUDA;
+    p.skip_first_load = 0;
+
+    CUtensorMap ta, tb;
+    if (!make_map(&ta, Xq, (uint64_t)K, (uint64_t)n_tokens, (uint64_t)K, BK, 1))  // gather4: one-row box
+        return FP8FG_ECUDA;
+    if (!make_map(&tb, Wq, (uint64_t)K, (uint64_t)n_experts * (uint64_t)N, (uint64_t)K, BK, BN))
+        return FP8FG_ECUDA;
+    const int grid = sm_count();
+    return launch_out<GROUPED>(out, ta, tb, p, grid > 0 ? grid : 1, static_cast<cudaStream_t>(stream));
+}

@@ -1,0 +1,294 @@
+// Fine-grained E4M3 quantisation kernels: 1x128 tiles (per row), 128x1 tiles
+// with transposed output (per column, for the weight-gradient operands), and
+// 128x128 blocks (weights).
+//
+// Group rule (innerforce.co.kr, fine-grained quantization paragraph, Figure
+// 7(a); tonho.wtf DeepSeek-V3 entry, "como funciona"): amax = max |x| over
+// the group; s = amax/448 and inv = 448/amax as IEEE FP32 divisions (s = inv
+// = 1 when amax is 0 or 448/amax overflows); code = E4M3(x*inv) with one FP32
+// product and one round-to-nearest-even, saturating conversion.
+//
+// All three kernels are HBM-bound streams (2 bytes read, 1 byte + 4/128 or
+// 4/16384 bytes written per element). They read with 16-byte vector loads
+// issued back to back (several in flight per thread), reduce the amax with
+// warp shuffles, and write codes and scales with full 32-byte sectors.
+#include <cuda_bf16.h>
+
+#include "host_common.h"
+#include "ptx.cuh"
+
+namespace fp8fg {
+namespace {
+
+constexpr int GROUP = 128;
+
+struct ScalePair {
+    float s, inv;
+};
+
+__device__ __forceinline__ ScalePair group_scale(float amax)
+{
+    ScalePair r{1.0f, 1.0f};
+    if (amax != 0.0f) {
+        float inv = __fdiv_rn(448.0f, amax);
+        if (!isinf(inv)) {
+            r.inv = inv;
+            r.s = __fdiv_rn(amax, 448.0f);
+        }
+    }
+    return r;
+}
+
+// max |x| over 8 bf16 values packed in a uint4 (bit patterns of magnitudes
+// order like the magnitudes themselves).
+__device__ __forceinline__ uint32_t absmax_bits8(const uint4 &v)
+{
+    uint32_t m = __vmaxu2(__vmaxu2(v.x & 0x7FFF7FFFu, v.y & 0x7FFF7FFFu),
+                          __vmaxu2(v.z & 0x7FFF7FFFu, v.w & 0x7FFF7FFFu));
+    return max(m & 0xFFFFu, m >> 16);
+}
+
+__device__ __forceinline__ uint32_t quant2(uint32_t w, float inv)
+{
+    return cvt_e4m3x2(__fmul_rn(bf16_lo(w), inv), __fmul_rn(bf16_hi(w), inv));
+}
+
+// 8 bf16 -> 8 E4M3 bytes
+__device__ __forceinline__ uint2 quant8(const uint4 &v, float inv)
+{
+    uint2 o;
+    o.x = quant2(v.x, inv) | (quant2(v.y, inv) << 16);
+    o.y = quant2(v.z, inv) | (quant2(v.w, inv) << 16);
+    return o;
+}
+
+__device__ __forceinline__ uint4 ld_stream_v4(const void *p)
+{
+    uint4 v;
+    asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+                 : "l"(p));
+    return v;
+}
+
+// ------------------------------------------------------ 1x128, per row ----
+// CTA tile: 32 rows x 4 groups (512 columns); 256 threads = 16 half-warps.
+// Item t = i*16 + half_warp (i = 0..7) is (row t/4, group t%4), so the two
+// half-warps of a warp read 512 contiguous bytes of one row per load.
+constexpr int QR_ROWS = 32;
+constexpr int QR_GROUPS = 4;
+constexpr int QR_ITEMS = QR_ROWS * QR_GROUPS / 16;
+
+__global__ void __launch_bounds__(256) quant_rows_kernel(const uint16_t *__restrict__ x, int64_t rows,
+                                                         int64_t ngroups, int64_t ldx, uint8_t *__restrict__ q,
+                                                         int64_t ldq, float *__restrict__ scales, int64_t ld_s)
+{
+    __shared__ float s_scale[QR_GROUPS][QR_ROWS];
+    const int hw = threadIdx.x >> 4;
+    const int l = threadIdx.x & 15;
+    const int64_t r0 = (int64_t)blockIdx.x * QR_ROWS;
+    const int64_t g0 = (int64_t)blockIdx.y * QR_GROUPS;
+
+    uint4 v[QR_ITEMS];
+#pragma unroll
+    for (int i = 0; i < QR_ITEMS; ++i) {
+        const int t = i * 16 + hw;
+        const int64_t row = r0 + (t >> 2), g = g0 + (t & 3);
+        if (row < rows && g < ngroups)
+            v[i] = ld_stream_v4(x + row * ldx + g * GROUP + l * 8);
+        else
+            v[i] = make_uint4(0, 0, 0, 0);
+    }
+#pragma unroll
+    for (int i = 0; i < QR_ITEMS; ++i) {
+        const int t = i * 16 + hw;
+        const int64_t row = r0 + (t >> 2), g = g0 + (t & 3);
+        uint32_t m = absmax_bits8(v[i]);
+#pragma unroll
+        for (int off = 8; off >= 1; off >>= 1)
+            m = max(m, __shfl_xor_sync(0xffffffffu, m, off));
+        const ScalePair sp = group_scale(__uint_as_float(m << 16));
+        if (row < rows && g < ngroups) {
+            *reinterpret_cast<uint2 *>(q + row * ldq + g * GROUP + l * 8) = quant8(v[i], sp.inv);
+            if (l == 0)
+                s_scale[t & 3][t >> 2] = sp.s;
+        }
+    }
+    __syncthreads();
+    if (threadIdx.x < QR_ROWS * QR_GROUPS) {
+        const int gg = threadIdx.x / QR_ROWS, rr = threadIdx.x % QR_ROWS;
+        const int64_t row = r0 + rr, g = g0 + gg;
+        if (row < rows && g < ngroups)
+            scales[g * ld_s + row] = s_scale[gg][rr];
+    }
+}
+
+// ---------------------------------------- 128x1 along rows, transposed ----
+// CTA tile: 128 rows (one group) x 64 columns, staged in shared memory.
+// Thread (c = tid % 64, part = tid / 64) reduces rows part*32..+31 of
+// column c, then writes those 32 codes as 32 contiguous bytes of row c of
+// the transposed output.
+constexpr int QT_COLS = 64;
+
+__global__ void __launch_bounds__(256) quant_cols_t_kernel(const uint16_t *__restrict__ x, int64_t rows,
+                                                           int64_t cols, int64_t ldx, uint8_t *__restrict__ qT,
+                                                           int64_t ldq, float *__restrict__ scales, int64_t ld_s)
+{
+    __shared__ __align__(16) uint16_t tile[GROUP][QT_COLS];
+    __shared__ uint32_t s_amax[4][QT_COLS];
+    const int tid = threadIdx.x;
+    const int64_t c0 = (int64_t)blockIdx.x * QT_COLS;
+    const int64_t r0 = (int64_t)blockIdx.y * GROUP;
+
+    uint4 v[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        const int chunk = i * 256 + tid;
+        const int rr = chunk >> 3, cc = (chunk & 7) * 8;
+        if (c0 + cc < cols)
+            v[i] = ld_stream_v4(x + (r0 + rr) * ldx + c0 + cc);
+        else
+            v[i] = make_uint4(0, 0, 0, 0);
+    }
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        const int chunk = i * 256 + tid;
+        *reinterpret_cast<uint4 *>(&tile[chunk >> 3][(chunk & 7) * 8]) = v[i];
+    }
+    __syncthreads();
+
+    const int c = tid & (QT_COLS - 1), part = tid >> 6;
+    uint32_t m = 0;
+#pragma unroll 8
+    for (int i = 0; i < 32; ++i)
+        m = max(m, (uint32_t)(tile[part * 32 + i][c] & 0x7FFFu));
+    s_amax[part][c] = m;
+    __syncthreads();
+    m = max(max(s_amax[0][c], s_amax[1][c]), max(s_amax[2][c], s_amax[3][c]));
+    const ScalePair sp = group_scale(__uint_as_float(m << 16));
+    const int64_t col = c0 + c;
+    if (col < cols) {
+        uint32_t packed[8];
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+            const int rb = part * 32 + j * 4;
+            const uint32_t lo = cvt_e4m3x2(__fmul_rn(__uint_as_float((uint32_t)tile[rb + 0][c] << 16), sp.inv),
+                                           __fmul_rn(__uint_as_float((uint32_t)tile[rb + 1][c] << 16), sp.inv));
+            const uint32_t hi = cvt_e4m3x2(__fmul_rn(__uint_as_float((uint32_t)tile[rb + 2][c] << 16), sp.inv),
+                                           __fmul_rn(__uint_as_float((uint32_t)tile[rb + 3][c] << 16), sp.inv));
+            packed[j] = lo | (hi << 16);
+        }
+        uint4 *dst = reinterpret_cast<uint4 *>(qT + col * ldq + r0 + part * 32);
+        dst[0] = make_uint4(packed[0], packed[1], packed[2], packed[3]);
+        dst[1] = make_uint4(packed[4], packed[5], packed[6], packed[7]);
+        if (part == 0)
+            scales[(r0 / GROUP) * ld_s + col] = sp.s;
+    }
+}
+
+// ------------------------------------------------------- 128x128 blocks ----
+// One CTA per block: 256 threads x 8 chunks of 8 bf16 held in registers.
+__global__ void __launch_bounds__(256) quant_blocks_kernel(const uint16_t *__restrict__ w, int64_t K, int64_t ldw,
+                                                           uint8_t *__restrict__ q, int64_t ldq,
+                                                           float *__restrict__ scales)
+{
+    __shared__ uint32_t s_warp[8];
+    const int tid = threadIdx.x;
+    const int64_t bj = blockIdx.x, bi = blockIdx.y;
+    const uint16_t *src = w + bi * GROUP * ldw + bj * GROUP;
+
+    uint4 v[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+        const int chunk = i * 256 + tid;  // 16 chunks of 8 per row
+        v[i] = ld_stream_v4(src + (chunk >> 4) * ldw + (chunk & 15) * 8);
+    }
+    uint32_t m = 0;
+#pragma unroll
+    for (int i = 0; i < 8; ++i)
+        m = max(m, absmax_bits8(v[i]));
+#pragma unroll
+    for (int off = 16; off >= 1; off >>= 1)
+        m = max(m, __shfl_xor_sync(0xffffffffu, m, off));
+    if ((tid & 31) == 0)
+        s_warp[tid >> 5] = m;
+    __syncthreads();
+    m = s_warp[0];
+#pragma unroll
+    for (int i = 1; i < 8; ++i)
+        m = max(m, s_warp[i]);
+    const ScalePair sp = group_scale(__uint_as_float(m << 16));
+    uint8_t *dst = q + bi * GROUP * ldq + bj * GROUP;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+        const int chunk = i * 256 + tid;
+        *reinterpret_cast<uint2 *>(dst + (chunk >> 4) * ldq + (chunk & 15) * 8) = quant8(v[i], sp.inv);
+    }
+    if (tid == 0)
+        scales[bi * (K / GROUP) + bj] = sp.s;
+}
+
+}  // namespace
+}  // namespace fp8fg
+
+using namespace fp8fg;
+
+extern "C" int fp8_quant_1x128(const void *x, int64_t rows, int64_t cols, int64_t ldx, uint8_t *q, int64_t ldq,
+                               float *scales, int64_t ld_s, int transpose, void *stream)
+{
+    if (rows < 0 || cols < 0 || (transpose != 0 && transpose != 1))
+        return FP8FG_EINVAL;
+    if (transpose == 0) {
+        if (cols % GROUP != 0 || ldx < cols || ldq < cols || ld_s < rows)
+            return FP8FG_EINVAL;
+    } else {
+        if (rows % GROUP != 0 || ldx < cols || ldq < rows || ld_s < cols)
+            return FP8FG_EINVAL;
+    }
+    if (rows == 0 || cols == 0)
+        return FP8FG_OK;
+    if (!x || !q || !scales)
+        return FP8FG_EINVAL;
+    if (!aligned16(x) || !aligned16(q) || !aligned16(scales) || ldx % 8 != 0 || ldq % 16 != 0 || ld_s % 4 != 0)
+        return FP8FG_EALIGN;
+    if (!device_supported())
+        return FP8FG_EUNSUPPORTED;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (transpose == 0) {
+        const int64_t ngroups = cols / GROUP;
+        const int64_t gx = (rows + QR_ROWS - 1) / QR_ROWS, gy = (ngroups + QR_GROUPS - 1) / QR_GROUPS;
+        if (gx > 0x7FFFFFFF || gy > 65535)
+            return FP8FG_EINVAL;
+        quant_rows_kernel<<<dim3((unsigned)gx, (unsigned)gy), 256, 0, s>>>(
+            static_cast<const uint16_t *>(x), rows, ngroups, ldx, q, ldq, scales, ld_s);
+    } else {
+        const int64_t gx = (cols + QT_COLS - 1) / QT_COLS, gy = rows / GROUP;
+        if (gx > 0x7FFFFFFF || gy > 65535)
+            return FP8FG_EINVAL;
+        quant_cols_t_kernel<<<dim3((unsigned)gx, (unsigned)gy), 256, 0, s>>>(
+            static_cast<const uint16_t *>(x), rows, cols, ldx, q, ldq, scales, ld_s);
+    }
+    return launch_status();
+}
+
+extern "C" int fp8_quant_128x128(const void *w, int64_t N, int64_t K, int64_t ldw, uint8_t *q, int64_t ldq,
+                                 float *scales, void *stream)
+{
+    if (N < 0 || K < 0 || N % GROUP != 0 || K % GROUP != 0 || ldw < K || ldq < K)
+        return FP8FG_EINVAL;
+    if (N == 0 || K == 0)
+        return FP8FG_OK;
+    if (!w || !q || !scales)
+        return FP8FG_EINVAL;
+    if (!aligned16(w) || !aligned16(q) || ldw % 8 != 0 || ldq % 16 != 0 ||
+        (reinterpret_cast<uintptr_t>(scales) & 3u) != 0)
+        return FP8FG_EALIGN;
+    if (!device_supported())
+        return FP8FG_EUNSUPPORTED;
+    const int64_t gx = K / GROUP, gy = N / GROUP;
+    if (gx > 0x7FFFFFFF || gy > 65535)
+        return FP8FG_EINVAL;
+    quant_blocks_kernel<<<dim3((unsigned)gx, (unsigned)gy), 256, 0, static_cast<cudaStream_t>(stream)>>>(
+        static_cast<const uint16_t *>(w), K, ldw, q, ldq, scales);
+    return launch_status();
+}

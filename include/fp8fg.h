@@ -1,0 +1,219 @@
+/*
+ * fp8fg.h - fine-grained FP8 quantisation and block-scaled FP8 GEMM on
+ * GB300 (sm_103a). C ABI of libfp8fg.so.
+ *
+ * What the operations compute comes from web pages describing DeepSeek-V3's
+ * FP8 mixed-precision training framework:
+ *   - innerforce.co.kr, paragraph on fine-grained quantization (Figure
+ *     7(a)): activations are scaled per 1x128 tile (one token, 128
+ *     channels), weights per 128x128 block; each group's largest magnitude
+ *     is mapped onto FP8's largest representable value. The following
+ *     paragraph: FP8 GEMM partial sums are promoted and accumulated in FP32,
+ *     and dequantisation rides on that promotion.
+ *   - yunhecapital.com, section 2.2.3 (FP8 mixed-precision framework):
+ *     the same 1x128 / 128x128 grouping; at each accumulation interval the
+ *     tensor-core partials move to FP32 registers on CUDA cores.
+ *   - tonho.wtf DeepSeek-V3 entry, section "como funciona": scale factors
+ *     are computed online, tensors are always E4M3, partials are promoted
+ *     every 128 elements. Section "o que isso custou": activation gradients
+ *     diverge under 128x128 blocks (so they use 1x128 tiles), and a fused
+ *     cast and a transposed read are on the hardware wish list.
+ *
+ * Numerics shared by every entry point:
+ *   E4M3      OCP FP8 E4M3 ("fn"): bias 7, no infinities, max finite +-448.
+ *   scale     per group: amax = max |x| over the group's bf16 values;
+ *             s = amax / 448 and inv = 448 / amax, both IEEE FP32 divisions
+ *             rounded to nearest. If amax == 0, or 448/amax overflows FP32,
+ *             s = inv = 1.
+ *   code      q = E4M3(x * inv): one FP32 product, then round to nearest
+ *             even into E4M3, saturating at +-448; the sign of zero is kept.
+ *   GEMM      C[i,j] = sum over 128-wide contraction blocks kb of
+ *             sA(i,kb) * sB(j,kb) * P(i,j,kb), P the block's FP8 x FP8 dot
+ *             product from the tensor cores (FP32 in tensor memory), the sum
+ *             over kb kept in FP32 registers.
+ *
+ * Conventions for every call:
+ *   - All pointers are DEVICE pointers owned by the caller. The library
+ *     allocates no device memory and keeps no state beyond per-device
+ *     kernel attributes and a device status word.
+ *   - `stream` is a cudaStream_t passed as void* (NULL = legacy default
+ *     stream). Work is enqueued asynchronously; no call synchronises.
+ *   - Leading dimensions are in ELEMENTS. Matrices are row-major.
+ *   - Synchronous validation returns FP8FG_EINVAL (null pointer, negative or
+ *     unsupported size, leading dimension too small), FP8FG_EALIGN (a pointer
+ *     not 16-byte aligned or a row pitch not a multiple of 16 bytes) before
+ *     anything is launched; FP8FG_ECUDA if a launch fails. A zero-sized
+ *     problem returns FP8FG_OK and launches nothing.
+ *   - Errors found on the device (a bounded wait that ran out, an expert row
+ *     index out of range) are recorded in a per-device status word and
+ *     reported by fp8fg_device_status(). Kernels never trap.
+ *   - No C++ exception crosses this interface.
+ */
+#ifndef FP8FG_H
+#define FP8FG_H
+
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define FP8FG_API __attribute__((visibility("default")))
+#else
+#define FP8FG_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    FP8FG_OK = 0,
+    FP8FG_EINVAL = 1,       /* invalid argument */
+    FP8FG_EALIGN = 2,       /* pointer or pitch not 16-byte aligned */
+    FP8FG_EUNSUPPORTED = 3, /* device is not sm_103 / feature unavailable */
+    FP8FG_ECUDA = 4,        /* CUDA runtime or driver error */
+    FP8FG_ETIMEOUT = 5,     /* a device-side bounded wait ran out */
+    FP8FG_EDEVICE = 6       /* invalid data found on the device */
+} fp8fg_status;
+
+typedef enum { FP8FG_OUT_F32 = 0, FP8FG_OUT_BF16 = 1 } fp8fg_out;
+
+typedef enum { FP8FG_FPROP = 0, FP8FG_DGRAD = 1, FP8FG_WGRAD = 2 } fp8fg_mode;
+
+/* ---------------------------------------------------------------------
+ * fp8_quant_1x128: activation quantisation in 1x128 tiles.
+ * Source: innerforce.co.kr, fine-grained quantization paragraph (Figure
+ * 7(a)), "per token per 128 channels"; tonho.wtf "como funciona" (online
+ * scale, E4M3); for transpose = 1, tonho.wtf "o que isso custou"
+ * (transposed read for the weight-gradient operands, which are grouped
+ * along tokens).
+ *
+ *   x       bf16 [rows][ldx], row-major, ldx >= cols.
+ *   transpose = 0: groups are 128 consecutive COLUMNS of one row.
+ *           cols % 128 == 0, rows >= 0 arbitrary.
+ *           q      E4M3 bytes [rows][ldq], ldq >= cols.
+ *           scales FP32 [cols/128][ld_s], ld_s >= rows: scale of row r,
+ *                  group g at scales[g*ld_s + r] (groups outer, rows
+ *                  contiguous: the layout the GEMM reads).
+ *   transpose = 1: groups are 128 consecutive ROWS of one column and the
+ *           output is transposed. rows % 128 == 0, cols >= 0 arbitrary.
+ *           q      E4M3 bytes [cols][ldq], ldq >= rows: q[c*ldq + r].
+ *           scales FP32 [rows/128][ld_s], ld_s >= cols: scale of column c,
+ *                  group g at scales[g*ld_s + c].
+ *           (This is exactly the transpose=0 output for the matrix x^T.)
+ *   Alignment: x, q, scales 16-byte aligned; ldx % 8 == 0, ldq % 16 == 0,
+ *   ld_s % 4 == 0.
+ * ------------------------------------------------------------------- */
+FP8FG_API int fp8_quant_1x128(const void *x, int64_t rows, int64_t cols, int64_t ldx,
+                    uint8_t *q, int64_t ldq, float *scales, int64_t ld_s,
+                    int transpose, void *stream);
+
+/* ---------------------------------------------------------------------
+ * fp8_quant_128x128: weight quantisation in 128x128 blocks.
+ * Source: innerforce.co.kr, fine-grained quantization paragraph ("per 128
+ * input channels per 128 output channels"); yunhecapital.com 2.2.3;
+ * tonho.wtf "como funciona".
+ *
+ *   w       bf16 [N][ldw], ldw >= K; N % 128 == 0, K % 128 == 0.
+ *   q       E4M3 bytes [N][ldq], ldq >= K.
+ *   scales  FP32 [N/128][K/128], dense: scale of block (i, j) at
+ *           scales[i*(K/128) + j].
+ *   Alignment: w, q 16-byte aligned; ldw % 8 == 0, ldq % 16 == 0.
+ * ------------------------------------------------------------------- */
+FP8FG_API int fp8_quant_128x128(const void *w, int64_t N, int64_t K, int64_t ldw,
+                      uint8_t *q, int64_t ldq, float *scales, void *stream);
+
+/* ---------------------------------------------------------------------
+ * fp8_gemm_blockscaled: block-scaled FP8 GEMM, promotion every 128 of the
+ * contraction dimension K.
+ * Source: innerforce.co.kr, increased-precision accumulation paragraph
+ * (FP32 accumulation, dequantisation folded into the promotion);
+ * yunhecapital.com 2.2.3; tonho.wtf "como funciona" (every 128 elements);
+ * tonho.wtf "o que isso custou" (activation gradients in 1x128 tiles).
+ *
+ * All modes compute C[M][N] (ldc >= N) with K % 128 == 0, N % 128 == 0,
+ * M >= 0 arbitrary; out = FP8FG_OUT_F32 (C is float) or FP8FG_OUT_BF16 (C
+ * is bf16, rounded to nearest even from the FP32 sum).
+ *
+ *   FP8FG_FPROP  C = A . B^T. A: activations quantised 1x128,
+ *                E4M3 [M][lda], scales sA [K/128][ld_sA] (ld_sA >= M).
+ *                B: weight quantised 128x128, E4M3 [N][ldb], scales
+ *                sB [N/128][ld_sB] (ld_sB >= K/128).
+ *   FP8FG_DGRAD  C = A . B. A: gradient dY quantised 1x128 along K (the
+ *                layer's output channels), [M][lda], sA [K/128][ld_sA].
+ *                B: the forward weight exactly as fp8_quant_128x128 stored
+ *                it, E4M3 [K][ldb] (ldb >= N), scales sB [K/128][ld_sB]
+ *                (ld_sB >= N/128). B is read N-contiguous; no transposed
+ *                copy is needed.
+ *   FP8FG_WGRAD  C = A . B^T with both operands quantised in groups of
+ *                128 along K (tokens), i.e. fp8_quant_1x128 outputs with
+ *                transpose = 1: A E4M3 [M][lda], sA [K/128][ld_sA]
+ *                (ld_sA >= M); B E4M3 [N][ldb], sB [K/128][ld_sB]
+ *                (ld_sB >= N). Each output element uses its row's and its
+ *                column's scale.
+ *   Alignment: A, B, C, sA, sB 16-byte aligned; lda, ldb % 16 == 0;
+ *   ldc*sizeof(out) % 16 == 0; ld_sA % 4 == 0 (and ld_sB % 4 == 0 for
+ *   WGRAD).
+ * ------------------------------------------------------------------- */
+FP8FG_API int fp8_gemm_blockscaled(int mode,
+                         const uint8_t *A, const float *sA, int64_t lda, int64_t ld_sA,
+                         const uint8_t *B, const float *sB, int64_t ldb, int64_t ld_sB,
+                         int64_t M, int64_t N, int64_t K,
+                         void *C, int out, int64_t ldc, void *stream);
+
+/* ---------------------------------------------------------------------
+ * fp8_grouped_gemm: MoE expert GEMM over a per-expert row index.
+ * Source: yunhecapital.com 2.2.2 and tonho.wtf "como funciona" (one shared
+ * and 256 routed experts, 8 active per token) with the FP8 GEMM above
+ * (expert GEMMs are FP8 GEMMs).
+ *
+ *   For each expert e and each row r in [off[e], off[e+1]):
+ *       Y[r][:] = fprop(Xq[row_index[r]], Wq[e])
+ *   Xq        E4M3 [n_tokens][K] (lda = K), quantised once per token 1x128.
+ *   sX        FP32 [K/128][ld_sX], ld_sX >= n_tokens (fp8_quant_1x128 layout).
+ *   row_index int32 [n_rows], device: token of each row, rows grouped by
+ *             expert. Entries outside [0, n_tokens) are reported as
+ *             FP8FG_EDEVICE through fp8fg_device_status and read token 0.
+ *   expert_offsets int32 [n_experts+1], device, non-decreasing, off[0] = 0,
+ *             off[n_experts] <= n_rows. Rows at or beyond off[n_experts] are
+ *             not written.
+ *   Wq        E4M3 [n_experts][N][K]; sW FP32 [n_experts][N/128][K/128].
+ *   Y         [n_rows][ldy], FP32 or bf16 per `out`.
+ *   K % 128 == 0, N % 128 == 0, 1 <= n_experts <= 4096.
+ *   Alignment: Xq, Wq, sX, Y 16-byte aligned; K % 16 == 0; ld_sX % 4 == 0;
+ *   ldy*sizeof(out) % 16 == 0.
+ * ------------------------------------------------------------------- */
+FP8FG_API int fp8_grouped_gemm(const uint8_t *Xq, const float *sX, int64_t ld_sX, int64_t n_tokens,
+                     const int32_t *row_index, const int32_t *expert_offsets,
+                     int32_t n_experts, int64_t n_rows,
+                     const uint8_t *Wq, const float *sW, int64_t N, int64_t K,
+                     void *Y, int out, int64_t ldy, void *stream);
+
+/* ---------------------------------------------------------------------
+ * Status and diagnostics (no counterpart on the pages).
+ * ------------------------------------------------------------------- */
+
+/* Human-readable name of a status code; never NULL. */
+FP8FG_API const char *fp8fg_status_str(int status);
+
+/* Synchronises `stream`, then returns and clears the current device's
+ * status word: FP8FG_OK, FP8FG_ETIMEOUT or FP8FG_EDEVICE (or FP8FG_ECUDA if
+ * the synchronisation itself failed). */
+FP8FG_API int fp8fg_device_status(void *stream);
+
+/* Library version (major*10000 + minor*100 + patch). */
+FP8FG_API int fp8fg_version(void);
+
+/* Test hook: when `skip` != 0, the next fp8_gemm_blockscaled launch on the
+ * current device withholds its first operand load, so the consumers' bounded
+ * waits run out and the launch reports FP8FG_ETIMEOUT. One-shot; returns
+ * FP8FG_OK. For exercising failure detection without a GPU fault. */
+FP8FG_API int fp8fg_test_skip_first_load(int skip);
+
+/* Wait limit of the device-side bounded waits, in nanoseconds (default two
+ * seconds). Values below 1e6 are raised to 1e6. Returns FP8FG_OK. */
+FP8FG_API int fp8fg_set_wait_limit_ns(int64_t ns);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* FP8FG_H */

@@ -1,0 +1,125 @@
+"""Host-side checks of the C ABI (no GPU): the library builds and loads,
+exports every function ``include/fp8fg.h`` declares, and rejects bad
+arguments before touching the device."""
+import ctypes
+import os
+import re
+
+import pytest
+
+import fp8_fine_grained_gb300 as fg
+from fp8_fine_grained_gb300 import build as libbuild
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "fp8fg.h")
+
+EINVAL, EALIGN, EUNSUPPORTED = 1, 2, 3
+
+
+@pytest.fixture(scope="module")
+def L():
+    libbuild.build()
+    return fg.lib()
+
+
+def declared_functions():
+    src = open(HEADER).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"FP8FG_API\s+[\w\s\*]+?\b(\w+)\s*\(", src)))
+
+
+def test_header_declares_the_four_entry_points():
+    names = declared_functions()
+    for n in ("fp8_quant_1x128", "fp8_quant_128x128", "fp8_gemm_blockscaled", "fp8_grouped_gemm"):
+        assert n in names
+
+
+def test_library_exports_every_declared_symbol(L):
+    raw = ctypes.CDLL(fg.LIB_PATH)
+    for n in declared_functions():
+        assert hasattr(raw, n), n
+
+
+def test_status_strings(L):
+    for code in range(7):
+        assert fg.status_str(code).startswith("FP8FG")
+    assert "unknown" in fg.status_str(99)
+
+
+# Fake, never-dereferenced device addresses: validation must fail first.
+A16 = ctypes.c_void_p(0x10000)
+A8 = ctypes.c_void_p(0x10008)
+NULL = None
+
+
+def q1x128(L, **kw):
+    a = dict(x=A16, rows=4, cols=256, ldx=256, q=A16, ldq=256, s=A16, lds=4, t=0)
+    a.update(kw)
+    return L.fp8_quant_1x128(a["x"], a["rows"], a["cols"], a["ldx"], a["q"], a["ldq"], a["s"], a["lds"], a["t"], NULL)
+
+
+def test_quant_1x128_validation(L):
+    assert q1x128(L, cols=200, ldx=200, ldq=200) == EINVAL          # cols % 128
+    assert q1x128(L, rows=-1) == EINVAL
+    assert q1x128(L, ldx=128) == EINVAL                              # ldx < cols
+    assert q1x128(L, lds=2) == EINVAL                                # ld_s < rows
+    assert q1x128(L, x=NULL) == EINVAL
+    assert q1x128(L, x=A8) == EALIGN
+    assert q1x128(L, ldx=260) == EALIGN
+    assert q1x128(L, t=2) == EINVAL
+    assert q1x128(L, t=1, rows=100) == EINVAL                        # transposed: rows % 128
+    assert q1x128(L, rows=0) == 0                                    # empty: nothing launched
+    assert q1x128(L) in (EUNSUPPORTED, 4)                            # valid args, no GPU here
+
+
+def test_quant_128x128_validation(L):
+    f = L.fp8_quant_128x128
+    assert f(A16, 100, 128, 128, A16, 128, A16, NULL) == EINVAL
+    assert f(A16, 128, 130, 130, A16, 130, A16, NULL) == EINVAL
+    assert f(A8, 128, 128, 128, A16, 128, A16, NULL) == EALIGN
+    assert f(A16, 0, 128, 128, A16, 128, A16, NULL) == 0
+
+
+def gemm(L, **kw):
+    a = dict(mode=0, A=A16, sA=A16, lda=256, ldsa=128, B=A16, sB=A16, ldb=256, ldsb=2, M=128, N=256, K=256,
+             C=A16, out=1, ldc=256)
+    a.update(kw)
+    return L.fp8_gemm_blockscaled(a["mode"], a["A"], a["sA"], a["lda"], a["ldsa"], a["B"], a["sB"], a["ldb"],
+                                  a["ldsb"], a["M"], a["N"], a["K"], a["C"], a["out"], a["ldc"], NULL)
+
+
+def test_gemm_validation(L):
+    assert gemm(L, mode=3) == EINVAL
+    assert gemm(L, out=2) == EINVAL
+    assert gemm(L, K=0) == EINVAL
+    assert gemm(L, K=200, lda=208, ldb=208) == EINVAL
+    assert gemm(L, N=200, ldc=208) == EINVAL
+    assert gemm(L, ldsa=100) == EINVAL                 # ld_sA < M
+    assert gemm(L, ldsb=1) == EINVAL                   # fprop: ld_sB < K/128
+    assert gemm(L, mode=2, ldsb=128) == EINVAL         # wgrad: ld_sB < N
+    assert gemm(L, mode=1, ldb=128, ldsb=2) == EINVAL  # dgrad: ldb < N
+    assert gemm(L, A=A8) == EALIGN
+    assert gemm(L, lda=264) == EALIGN
+    assert gemm(L, C=NULL) == EINVAL
+    assert gemm(L, M=0) == 0
+    assert gemm(L) in (EUNSUPPORTED, 4)
+
+
+def test_grouped_validation(L):
+    f = L.fp8_grouped_gemm
+
+    def call(**kw):
+        a = dict(X=A16, sX=A16, ldsx=64, T=64, ri=A16, off=A16, E=4, R=100, W=A16, sW=A16, N=256, K=256,
+                 Y=A16, out=1, ldy=256)
+        a.update(kw)
+        return f(a["X"], a["sX"], a["ldsx"], a["T"], a["ri"], a["off"], a["E"], a["R"], a["W"], a["sW"], a["N"],
+                 a["K"], a["Y"], a["out"], a["ldy"], NULL)
+
+    assert call(E=0) == EINVAL
+    assert call(E=5000) == EINVAL
+    assert call(K=100) == EINVAL
+    assert call(ldsx=32) == EINVAL
+    assert call(off=NULL) == EINVAL
+    assert call(X=A8) == EALIGN
+    assert call(R=0) == 0
+    assert call() in (EUNSUPPORTED, 4)

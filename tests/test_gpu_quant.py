@@ -1,0 +1,113 @@
+"""GPU parity of the quantisation kernels against the CPU oracle: codes and
+scales must match bit for bit (every case on the same seeded bf16 input)."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from fp8_fine_grained_gb300 import synth
+from tests.gpu_util import assert_quant_1x128, bits, to_np
+
+pytestmark = pytest.mark.gpu
+
+fg = pytest.importorskip("fp8_fine_grained_gb300")
+DEV = "cuda"
+
+
+def _x(rows, cols, seed, std=1.0):
+    g = torch.Generator(device=DEV)
+    g.manual_seed(seed)
+    c = torch.exp(torch.randn(cols, generator=g, device=DEV))
+    return (torch.randn(rows, cols, generator=g, device=DEV) * c * std).to(torch.bfloat16)
+
+
+@pytest.mark.parametrize("rows,cols", [(1, 128), (31, 256), (32, 512), (33, 640), (127, 128), (129, 1024),
+                                       (300, 896), (1000, 7168)])
+def test_quant_1x128_rows(rows, cols):
+    x = _x(rows, cols, seed=rows * 7 + cols)
+    q, s = fg.fp8_quant_1x128(x)
+    torch.cuda.synchronize()
+    assert_quant_1x128(x, q, s)
+
+
+def test_quant_1x128_strided_input_and_padded_outputs():
+    base = _x(70, 384 + 64, seed=3)
+    x = base[:, :384]                     # ldx = 448
+    q = torch.full((70, 512), 0xAA, dtype=torch.uint8, device=DEV)   # ldq = 512
+    s = torch.full((3, 76), -1.0, dtype=torch.float32, device=DEV)     # ld_s = 76
+    fg.fp8_quant_1x128(x, q=q[:, :384], scales=s)
+    torch.cuda.synchronize()
+    assert_quant_1x128(x.contiguous(), q[:, :384], s)
+    assert torch.all(q[:, 384:] == 0xAA) and torch.all(s[:, 70:] == -1.0)   # padding untouched
+
+
+def test_quant_1x128_special_values():
+    rows, cols = 8, 512
+    x = torch.zeros(rows, cols, dtype=torch.float32)
+    x[1, :128] = -0.0                               # all-zero group with negative zeros
+    x[2, 5] = 2.0 ** -133                           # smallest bf16 subnormal: 448/amax overflows
+    x[3, :] = 448.0 * 2.0 ** -3                     # amax = 448 * 2^e
+    x[4, 128:256] = torch.linspace(-3e38, 3e38, 128)  # near the bf16 maximum
+    x[5, :] = torch.arange(cols) * 1e-30            # tiny normals
+    x[6, 256:] = 1e-39                              # fp32 subnormal inputs
+    x[7, :] = torch.tensor([(-1.0) ** i * (i % 17) for i in range(cols)])
+    xb = x.to(torch.bfloat16).to(DEV)
+    q, s = fg.fp8_quant_1x128(xb)
+    torch.cuda.synchronize()
+    assert_quant_1x128(xb, q, s)
+
+
+@pytest.mark.parametrize("rows,cols", [(128, 1), (128, 64), (128, 100), (256, 200), (384, 640), (1024, 7168)])
+def test_quant_transposed(rows, cols):
+    x = _x(rows, cols, seed=rows + cols)
+    q, s = fg.fp8_quant_1x128(x, transpose=True)
+    torch.cuda.synchronize()
+    qo, so = oracle.quant_128x1_t(bits(x))
+    assert np.array_equal(to_np(q), qo)
+    assert np.array_equal(to_np(s)[:, :cols].view(np.uint32), so.view(np.uint32))
+
+
+@pytest.mark.parametrize("N,K", [(128, 128), (384, 640), (1024, 7168)])
+def test_quant_128x128(N, K):
+    g = torch.Generator(device=DEV)
+    g.manual_seed(N + K)
+    w = (torch.randn(N, K, generator=g, device=DEV) * 0.02)
+    w[:128, :128] *= 50
+    w[128:, :128] = 0.0 if N > 128 else w[128:, :128]
+    w = w.to(torch.bfloat16)
+    q, s = fg.fp8_quant_128x128(w)
+    torch.cuda.synchronize()
+    qo, so = oracle.quant_128x128(bits(w))
+    assert np.array_equal(to_np(q), qo)
+    assert np.array_equal(to_np(s).view(np.uint32), so.view(np.uint32))
+
+
+def test_quant_128x128_experts_3d():
+    g = torch.Generator(device=DEV)
+    g.manual_seed(5)
+    w = (torch.randn(3, 256, 384, generator=g, device=DEV) * 0.02).to(torch.bfloat16)
+    q, s = fg.fp8_quant_128x128(w)
+    torch.cuda.synchronize()
+    for e in range(3):
+        qo, so = oracle.quant_128x128(bits(w[e]))
+        assert np.array_equal(to_np(q[e]), qo)
+        assert np.array_equal(to_np(s[e]), so)
+
+
+def test_quant_dense_full_size():
+    """Full-size activation of the dense projection workload (4096 x 7168,
+    log-normal channel magnitudes), bit-exact against the oracle."""
+    x, w = synth.dense(seed=0, device=DEV)
+    q, s = fg.fp8_quant_1x128(x)
+    torch.cuda.synchronize()
+    assert_quant_1x128(x, q, s)
+    wq, sw = fg.fp8_quant_128x128(w)
+    torch.cuda.synchronize()
+    qo, so = oracle.quant_128x128(bits(w))
+    assert np.array_equal(to_np(wq), qo) and np.array_equal(to_np(sw), so)
+
+
+def test_quant_zero_size_is_noop():
+    x = torch.empty(0, 256, dtype=torch.bfloat16, device=DEV)
+    q, s = fg.fp8_quant_1x128(x)
+    assert q.shape == (0, 256)
