@@ -50,6 +50,7 @@ def lib():
         L.orc_quant_128x128.argtypes = [P, I64, I64, P, P]
         L.orc_gemm_blockscaled.argtypes = [P, P, P, P, I64, I64, I64, P, I64, P, P, P]
         L.orc_f32_to_bf16.argtypes = [P, I64, P]
+        L.orc_num_threads.restype = ctypes.c_int
         _lib = L
     return _lib
 
@@ -234,6 +235,11 @@ def grouped(xq, sx, row_index, expert_offsets, wq, sw, rows=None, want_exact=Tru
             ce[pick] = cei
             tl[pick] = tli
     return (c, ce, tl) if want_exact else (c, None, None)
+
+
+def num_threads():
+    """Threads the oracle's OpenMP regions run on."""
+    return int(lib().orc_num_threads())
 
 
 def to_bf16_bits(c):

@@ -45,6 +45,8 @@
 #include <stdint.h>
 #include <string.h>
 
+#include <omp.h>
+
 #define ORC_GROUP 128
 
 /* ---------------------------------------------------------------------- */
@@ -307,3 +309,15 @@ void orc_f32_to_bf16(const float *v, int64_t n, uint16_t *out)
 }
 
 int orc_version(void) { return 1; }
+
+/* Threads an OpenMP parallel region of this library uses. */
+int orc_num_threads(void)
+{
+    int n = 1;
+#pragma omp parallel
+    {
+#pragma omp single
+        n = omp_get_num_threads();
+    }
+    return n;
+}

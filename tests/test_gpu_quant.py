@@ -47,7 +47,7 @@ def test_quant_1x128_special_values():
     x[1, :128] = -0.0                               # all-zero group with negative zeros
     x[2, 5] = 2.0 ** -133                           # smallest bf16 subnormal: 448/amax overflows
     x[3, :] = 448.0 * 2.0 ** -3                     # amax = 448 * 2^e
-    x[4, 128:256] = torch.linspace(-3e38, 3e38, 128)  # near the bf16 maximum
+    x[4, 128:256] = torch.linspace(-1.0, 1.0, 128) * 3e38  # near the bf16 maximum (finite)
     x[5, :] = torch.arange(cols) * 1e-30            # tiny normals
     x[6, 256:] = 1e-39                              # fp32 subnormal inputs
     x[7, :] = torch.tensor([(-1.0) ** i * (i % 17) for i in range(cols)])
@@ -59,7 +59,10 @@ def test_quant_1x128_special_values():
 
 @pytest.mark.parametrize("rows,cols", [(128, 1), (128, 64), (128, 100), (256, 200), (384, 640), (1024, 7168)])
 def test_quant_transposed(rows, cols):
-    x = _x(rows, cols, seed=rows + cols)
+    # the row pitch must be a multiple of 8 elements: ragged widths are views
+    # into a wider buffer
+    pitch = (cols + 7) // 8 * 8
+    x = _x(rows, pitch, seed=rows + cols)[:, :cols]
     q, s = fg.fp8_quant_1x128(x, transpose=True)
     torch.cuda.synchronize()
     qo, so = oracle.quant_128x1_t(bits(x))
