@@ -17,12 +17,15 @@
 //               4 x tcgen05.mma (M128 N256 K32, E4M3 -> FP32) per block into
 //               one of two 256-column TMEM partial buffers, and commits to
 //               the stage's "empty" and the buffer's "full" barrier.
-//   warps 2..9  promotion/epilogue: each thread owns one output row and 128
+//   warps 2..3  complete warpgroup 0 (no role) so that setmaxnreg can move
+//               its registers to the promotion warpgroups.
+//   warps 4..11 promotion/epilogue: each thread owns one output row and 128
 //               columns; per block it loads the partial from TMEM
-//               (tcgen05.ld 32x32b), does acc = fma(P, sA*sB, acc) in FP32
-//               registers and frees the TMEM buffer, so the MMA of block
-//               kb+1 overlaps the promotion of block kb. After the last
-//               block it rounds and stores the row.
+//               (tcgen05.ld 32x32b, 32 columns at a time, two loads in
+//               flight), does acc = fma(P, sA*sB, acc) in FP32 registers
+//               (paired FP32 FMAs) and frees the TMEM buffer, so the MMA of
+//               block kb+1 overlaps the promotion of block kb. After the
+//               last block it rounds and stores the row.
 // Every wait is bounded (global timer); a wait that runs out records
 // FP8FG_ETIMEOUT in the device status word and all roles leave their loops,
 // drain their own in-flight copies and MMAs, and release tensor memory.
@@ -39,7 +42,17 @@ constexpr int BN = 256;        // output columns per tile
 constexpr int BK = 128;        // contraction block = promotion interval = scale group
 constexpr int STAGES = 4;
 constexpr int EPI_WARPS = 8;
-constexpr int NUM_THREADS = (2 + EPI_WARPS) * 32;
+constexpr int EPI_WARP0 = 4;                  // promotion warps are warpgroups 1 and 2
+constexpr int NUM_THREADS = (EPI_WARP0 + EPI_WARPS) * 32;
+constexpr int CHUNK = 32;                     // TMEM columns per tcgen05.ld in the promotion loop
+// Register split (setmaxnreg): warpgroup 0 (TMA, MMA and two idle warps)
+// gives registers to the two promotion warpgroups, which hold 128 FP32 sums
+// per thread plus two 32-column partial buffers. The launch holds
+// NUM_THREADS x (compiled register count) registers; the split must fit in
+// it, which the host checks before every launch.
+constexpr int LOW_REGS = 40;
+constexpr int EPI_REGS = 224;
+constexpr int LAUNCH_REGS_MIN = (4 * 32 * LOW_REGS + EPI_WARPS * 32 * EPI_REGS + NUM_THREADS - 1) / NUM_THREADS;
 constexpr uint32_t A_STAGE_BYTES = BM * BK;   // 16 KB
 constexpr uint32_t B_STAGE_BYTES = BN * BK;   // 32 KB
 constexpr uint32_t TMEM_COLS = 512;           // two 256-column partial buffers
@@ -244,6 +257,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 
     if (warp == 0) {
         // ------------------------------------------------------ producer ----
+        setmaxnreg_dec<LOW_REGS>();
         uint32_t stage = 0, phase = 0;
         uint32_t filled_mask = 0, fill_parity = 0;  // per stage: a fill was issued, and its parity
         bool skip = p.skip_first_load && blockIdx.x == 0;
@@ -328,6 +342,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         }
     } else if (warp == 1) {
         // ---------------------------------------------------------- MMA ----
+        setmaxnreg_dec<LOW_REGS>();
         if (lane == 0) {
             constexpr uint32_t IDESC = idesc_e4m3_f32(BM, BN, MODE == DGRAD);
             uint32_t stage = 0, phase = 0, buf = 0, tphase = 0;
@@ -386,9 +401,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             }
         }
         __syncwarp();
-    } else {
+    } else if (warp >= EPI_WARP0) {
         // ------------------------------------------ promotion / epilogue ----
-        const int ew = warp - 2;
+        setmaxnreg_inc<EPI_REGS>();
+        const int ew = warp - EPI_WARP0;
         const int quarter = warp & 3;        // TMEM lanes 32*quarter .. +31
         const int half = ew >> 2;            // output columns half*128 .. +127 of the tile
         const int row_in_tile = quarter * 32 + lane;
@@ -425,10 +441,11 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 return __ldg(reinterpret_cast<const float4 *>(p.sB + (int64_t)kb * p.ld_sB + col0) + lane);
             };
 
-            float acc[128];
+            // running FP32 sums of this thread's row, 128 columns as 64 pairs
+            float2 acc[64];
 #pragma unroll
-            for (int j = 0; j < 128; ++j)
-                acc[j] = 0.0f;
+            for (int j = 0; j < 64; ++j)
+                acc[j] = make_float2(0.0f, 0.0f);
             float sa_next = load_sa(0);
             float sb_next = 0.0f;
             float4 sbv_next = make_float4(0.f, 0.f, 0.f, 0.f);
@@ -460,29 +477,31 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 tc_fence_after();
                 const uint32_t taddr = tmem_base + ((uint32_t)(quarter * 32) << 16) + buf * BN + half * 128;
                 const float s = sa * sb;
-                uint32_t r[2][16];
-                tmem_ld16(taddr, r[0]);
-                tmem_wait_ld_into(r[0]);
+                const float2 s2 = make_float2(s, s);
+                const float2 sa2 = make_float2(sa, sa);
+                // two loads in flight: chunk c+1 streams from TMEM while chunk
+                // c is folded in with paired FP32 FMAs
+                uint32_t r[2][CHUNK];
+                tmem_ld_chunk(taddr, r[0]);
+                tmem_wait_ld_chunk(r[0]);
 #pragma unroll
-                for (int c = 0; c < 8; ++c) {
-                    if (c + 1 < 8)
-                        tmem_ld16(taddr + (c + 1) * 16, r[(c + 1) & 1]);
-                    if constexpr (MODE == WGRAD) {
+                for (int c = 0; c < 128 / CHUNK; ++c) {
+                    if (c + 1 < 128 / CHUNK)
+                        tmem_ld_chunk(taddr + (c + 1) * CHUNK, r[(c + 1) & 1]);
 #pragma unroll
-                        for (int j = 0; j < 16; j += 4) {
-                            const float4 sc = reinterpret_cast<const float4 *>(wscale)[(c * 16 + j) >> 2];
-                            acc[c * 16 + j + 0] = fmaf(__uint_as_float(r[c & 1][j + 0]), sa * sc.x, acc[c * 16 + j + 0]);
-                            acc[c * 16 + j + 1] = fmaf(__uint_as_float(r[c & 1][j + 1]), sa * sc.y, acc[c * 16 + j + 1]);
-                            acc[c * 16 + j + 2] = fmaf(__uint_as_float(r[c & 1][j + 2]), sa * sc.z, acc[c * 16 + j + 2]);
-                            acc[c * 16 + j + 3] = fmaf(__uint_as_float(r[c & 1][j + 3]), sa * sc.w, acc[c * 16 + j + 3]);
+                    for (int j = 0; j < CHUNK / 2; ++j) {
+                        const float2 pv =
+                            make_float2(__uint_as_float(r[c & 1][2 * j]), __uint_as_float(r[c & 1][2 * j + 1]));
+                        const int a = c * (CHUNK / 2) + j;
+                        if constexpr (MODE == WGRAD) {
+                            const float2 sc = reinterpret_cast<const float2 *>(wscale)[a];
+                            acc[a] = __ffma2_rn(pv, __fmul2_rn(sa2, sc), acc[a]);
+                        } else {
+                            acc[a] = __ffma2_rn(pv, s2, acc[a]);
                         }
-                    } else {
-#pragma unroll
-                        for (int j = 0; j < 16; ++j)
-                            acc[c * 16 + j] = fmaf(__uint_as_float(r[c & 1][j]), s, acc[c * 16 + j]);
                     }
-                    if (c + 1 < 8)
-                        tmem_wait_ld_into(r[(c + 1) & 1]);
+                    if (c + 1 < 128 / CHUNK)
+                        tmem_wait_ld_chunk(r[(c + 1) & 1]);
                 }
                 tc_fence_before();
                 __syncwarp();
@@ -499,26 +518,29 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 if constexpr (OUT_BF16) {
                     uint4 *dst = reinterpret_cast<uint4 *>(static_cast<__nv_bfloat16 *>(p.C) + row * p.ldc + col0);
 #pragma unroll
-                    for (int j = 0; j < 128; j += 8) {
+                    for (int j = 0; j < 64; j += 4) {
                         uint4 o;
-                        __nv_bfloat162 h0 = __floats2bfloat162_rn(acc[j + 0], acc[j + 1]);
-                        __nv_bfloat162 h1 = __floats2bfloat162_rn(acc[j + 2], acc[j + 3]);
-                        __nv_bfloat162 h2 = __floats2bfloat162_rn(acc[j + 4], acc[j + 5]);
-                        __nv_bfloat162 h3 = __floats2bfloat162_rn(acc[j + 6], acc[j + 7]);
+                        __nv_bfloat162 h0 = __float22bfloat162_rn(acc[j + 0]);
+                        __nv_bfloat162 h1 = __float22bfloat162_rn(acc[j + 1]);
+                        __nv_bfloat162 h2 = __float22bfloat162_rn(acc[j + 2]);
+                        __nv_bfloat162 h3 = __float22bfloat162_rn(acc[j + 3]);
                         o.x = *reinterpret_cast<uint32_t *>(&h0);
                         o.y = *reinterpret_cast<uint32_t *>(&h1);
                         o.z = *reinterpret_cast<uint32_t *>(&h2);
                         o.w = *reinterpret_cast<uint32_t *>(&h3);
-                        dst[j / 8] = o;
+                        dst[j / 4] = o;
                     }
                 } else {
                     float4 *dst = reinterpret_cast<float4 *>(static_cast<float *>(p.C) + row * p.ldc + col0);
 #pragma unroll
-                    for (int j = 0; j < 128; j += 4)
-                        dst[j / 4] = make_float4(acc[j], acc[j + 1], acc[j + 2], acc[j + 3]);
+                    for (int j = 0; j < 64; j += 2)
+                        dst[j / 2] = make_float4(acc[j].x, acc[j].y, acc[j + 1].x, acc[j + 1].y);
                 }
             }
         }
+    } else {
+        // warps 2..3 complete warpgroup 0 and have no role
+        setmaxnreg_dec<LOW_REGS>();
     }
 
     tc_fence_before();
@@ -577,6 +599,15 @@ int launch(const CUtensorMap &ta, const CUtensorMap &tb, const Params &p, int gr
         cudaGetLastError();
         return FP8FG_ECUDA;
     }
+    // The setmaxnreg split must fit in the registers the launch holds, or
+    // the promotion warps' increase would never be granted.
+    cudaFuncAttributes fa;
+    if (cudaFuncGetAttributes(&fa, k) != cudaSuccess) {
+        cudaGetLastError();
+        return FP8FG_ECUDA;
+    }
+    if (fa.numRegs < LAUNCH_REGS_MIN)
+        return FP8FG_EUNSUPPORTED;
     k<<<grid, NUM_THREADS, SmemLayout::total, s>>>(ta, tb, p);
     return launch_status();
 }
