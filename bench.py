@@ -1,22 +1,37 @@
 """Benchmark of the fine-grained FP8 hot path on GB300.
 
-One step = 1x128 quantisation of the activation X (bf16 -> E4M3 + FP32
-scales) followed by the block-scaled FP8 GEMM Y = X W^T (bf16 out), on the
-dense projection workload: M = 4096 tokens, K = N = 7168, X with log-normal
-per-channel magnitudes, W ~ N(0, 0.02) quantised once in 128x128 blocks
-before timing (weights change once per optimiser step, not per GEMM). The
-metric is whole-job TFLOP/s (2*M*N*K per step) on the device with inputs
-resident in HBM; ``e2e`` adds the host->device copy of X and the
-device->host copy of Y (pinned host buffers) inside the timed region.
+Default workload (``--workload dense``): one step = 1x128 quantisation of the
+activation X (bf16 -> E4M3 + FP32 scales) followed by the block-scaled FP8
+GEMM Y = X W^T (bf16 out) for a dense projection with M = 4096 tokens and
+K = N = 7168. X has log-normal per-channel magnitudes, W ~ N(0, 0.02) is
+quantised once in 128x128 blocks before timing (weights change once per
+optimiser step, not per GEMM). The metric is whole-job TFLOP/s (2*M*N*K per
+step) on the device with inputs resident in HBM; ``e2e`` adds the
+host->device copy of X and the device->host copy of Y (pinned host buffers)
+inside the timed region.
+
+Other workloads, one JSON line each, for the remaining kernels:
+    trio      linear layer 7168 -> 18432 at M = 8192: weight quantise, X and
+              dY quantised row-wise and transposed, fprop, dgrad, wgrad
+    moe       4096 tokens, 256 experts (2048 x 7168), top-8 with a Zipf(1.1)
+              expert bias: X quantise + grouped expert GEMM
+    outliers  M = 16384 fprop with outlier channels and weight blocks
+    tiny      128 x 256 x 128 fprop, FP32 out (latency)
+
+Every kernel of a step is timed with CUDA events on the launching stream; L2
+is flushed between steps (a 512 MiB write, then a 256 MiB read so that no
+dirty lines are written back inside the next step), outside the events.
 
 Usage:
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                    [--workload dense|trio|moe|outliers|tiny]
 Under torchrun (N > 1) every rank runs its own replica of the workload
-(weak scaling, no data-path collective); the step time is the max over ranks.
+(weak scaling, no data-path collective); times are the max over ranks.
 ``--impl reference`` times the CPU oracle on a bounded sample of the same
 workload (rank 0 only).
 """
 import argparse
+import hashlib
 import json
 import os
 import statistics
@@ -29,10 +44,18 @@ if ROOT not in sys.path:
     sys.path.insert(0, ROOT)
 
 METRIC = "block-scaled FP8 GEMM TFLOP/s (% FP8 peak); quantize GB/s (% HBM)"
-M, K, N = 4096, 7168, 7168
-WORKLOAD = "dense projection fprop: quant 1x128 + block-scaled GEMM, M=4096 K=7168 N=7168, bf16 out"
 L2_FLUSH_BYTES = 512 << 20
-QUANT_BYTES_PER_ELEM = 2 + 1 + 4.0 / 128      # read bf16, write E4M3, write one FP32 scale per 128
+L2_CLEAN_BYTES = 256 << 20
+Q1X128_B = 2 + 1 + 4.0 / 128       # bytes per element: read bf16, write E4M3, one FP32 scale per 128
+Q128X128_B = 2 + 1 + 4.0 / 16384   # one FP32 scale per 128x128 block
+
+WORKLOADS = {
+    "dense": "dense projection fprop: quant 1x128 + block-scaled GEMM, M=4096 K=7168 N=7168, bf16 out",
+    "trio": "linear 7168->18432 at M=8192: quant W 128x128, X/dY 1x128 and transposed; fprop, dgrad, wgrad",
+    "moe": "MoE experts: 4096 tokens, 256 experts 2048x7168, top-8 with Zipf(1.1) bias; quant X + grouped GEMM",
+    "outliers": "outlier-heavy fprop: quant 1x128 + block-scaled GEMM, M=16384 K=7168 N=7168, bf16 out",
+    "tiny": "tiny fprop: quant X 1x128 + quant W 128x128 + GEMM, 128x256x128, FP32 out",
+}
 
 
 def peaks():
@@ -40,9 +63,9 @@ def peaks():
     try:
         with open(path) as f:
             d = json.load(f)
-        return float(d["hbm_gbs"]), float(d["bf16_tflops"]), float(d.get("bf16_tflops_sustained", d["bf16_tflops"])), "measured"
+        return float(d["hbm_gbs"]), float(d["bf16_tflops"]), "measured"
     except (OSError, KeyError, ValueError):
-        return 6800.0, 1900.0, 1700.0, "fallback"
+        return 6800.0, 1900.0, "fallback"
 
 
 def dist_env():
@@ -52,6 +75,18 @@ def dist_env():
     return world, rank, local
 
 
+def reduce_max(values, pg):
+    """Element-wise max of a list of floats over all ranks (identity without a group)."""
+    if pg is None:
+        return list(values)
+    import torch
+    backend = pg.get_backend()
+    dev = torch.device("cuda", torch.cuda.current_device()) if backend == "nccl" else torch.device("cpu")
+    t = torch.tensor(list(values), dtype=torch.float64, device=dev)
+    pg.all_reduce(t, op=pg.ReduceOp.MAX)
+    return [float(v) for v in t.tolist()]
+
+
 class ClockSampler:
     """nvidia-smi clock/throttle sampling during the timed region."""
 
@@ -59,6 +94,7 @@ class ClockSampler:
         self.index = index
         self.out_path = out_path
         self.proc = None
+        self.f = None
 
     def __enter__(self):
         try:
@@ -68,7 +104,7 @@ class ClockSampler:
                  "--query-gpu=clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
                  "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
                  "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap",
-                 "--format=csv,noheader,nounits", "-lms", "100"],
+                 "--format=csv,noheader,nounits", "-lms", "50"],
                 stdout=self.f, stderr=subprocess.DEVNULL)
         except OSError:
             self.proc = None
@@ -82,31 +118,170 @@ class ClockSampler:
                 self.proc.wait(timeout=5)
             except subprocess.TimeoutExpired:
                 self.proc.kill()
-        self.f.close()
+        if self.f is not None:
+            self.f.close()
 
     def summary(self):
-        sm, mx, reasons = [], 0.0, set()
-        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        try:
-            for line in open(self.out_path):
-                parts = [p.strip() for p in line.split(",")]
-                if len(parts) < 8:
-                    continue
-                try:
-                    sm.append(float(parts[0]))
-                    mx = max(mx, float(parts[1]))
-                except ValueError:
-                    continue
-                for n, v in zip(names, parts[4:8]):
-                    if v.lower() == "active":
-                        reasons.add(n)
-        except OSError:
-            pass
-        if not sm:
-            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"], "samples": 0}
-        loaded = [v for v in sm if v > 0.5 * mx] or sm
-        return {"sm_mhz": statistics.median(loaded), "sm_max_mhz": mx, "reasons": sorted(reasons),
-                "samples": len(sm)}
+        return summarize_clocks(self.out_path)
+
+
+def summarize_clocks(path):
+    sm, mx, reasons = [], 0.0, set()
+    names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+    try:
+        for line in open(path):
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 8:
+                continue
+            try:
+                sm.append(float(parts[0]))
+                mx = max(mx, float(parts[1]))
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[4:8]):
+                if v.lower() == "active":
+                    reasons.add(n)
+    except OSError:
+        pass
+    if not sm:
+        return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"], "samples": 0}
+    loaded = [v for v in sm if v > 0.5 * mx] or sm
+    return {"sm_mhz": statistics.median(loaded), "sm_max_mhz": mx, "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# --------------------------------------------------------------- workloads ----
+
+class Part:
+    """One kernel of a step: a launch, its bound and its algorithmic units
+    (bytes for HBM-bound kernels, flops for tensor-bound ones)."""
+
+    def __init__(self, name, kernel, fn, bound, units, extra_bytes=None):
+        self.name, self.kernel, self.fn, self.bound, self.units = name, kernel, fn, bound, units
+        self.extra_bytes = extra_bytes   # grouped GEMM: bytes moved, reported beside the flops
+
+
+def build(workload, dev, seed, fg, synth):
+    """Device tensors, the step's parts, the metric's flops per step and the
+    host copies of e2e (inputs to upload, outputs to download)."""
+    import torch
+    W = {}
+    if workload in ("dense", "outliers", "tiny"):
+        if workload == "dense":
+            x, w = synth.dense(seed=seed, device=dev)
+        elif workload == "outliers":
+            x, w, _, _ = synth.outliers(seed=seed, device=dev)
+        else:
+            x, w = synth.tiny(seed=seed, device=dev)
+        Mx, Kx = x.shape
+        Nw = w.shape[0]
+        out_dt = torch.float32 if workload == "tiny" else torch.bfloat16
+        xq = torch.empty((Mx, Kx), dtype=torch.uint8, device=dev)
+        sx = torch.empty((Kx // 128, (Mx + 3) // 4 * 4), dtype=torch.float32, device=dev)
+        wq = torch.empty((Nw, Kx), dtype=torch.uint8, device=dev)
+        sw = torch.empty((Nw // 128, Kx // 128), dtype=torch.float32, device=dev)
+        y = torch.empty((Mx, Nw), dtype=out_dt, device=dev)
+        parts = [Part("quant_x_1x128", "quant_rows_kernel", lambda: fg.fp8_quant_1x128(x, q=xq, scales=sx),
+                      "hbm", Q1X128_B * Mx * Kx)]
+        if workload == "tiny":
+            parts.append(Part("quant_w_128x128", "quant_blocks_kernel",
+                              lambda: fg.fp8_quant_128x128(w, q=wq, scales=sw), "hbm", Q128X128_B * Nw * Kx))
+        else:
+            fg.fp8_quant_128x128(w, q=wq, scales=sw)
+        parts.append(Part("fprop", "gemm_kernel<FPROP>", lambda: fg.fprop(xq, sx, wq, sw, c=y), "tensor",
+                          2.0 * Mx * Nw * Kx))
+        W.update(inputs=[x], outputs=[y], flops=2.0 * Mx * Nw * Kx,
+                 dims={"M": Mx, "K": Kx, "N": Nw})
+    elif workload == "trio":
+        x, w, dy = synth.trio(seed=seed, device=dev)
+        Mx, Kx = x.shape
+        Nw = w.shape[0]
+        wq = torch.empty((Nw, Kx), dtype=torch.uint8, device=dev)
+        sw = torch.empty((Nw // 128, Kx // 128), dtype=torch.float32, device=dev)
+        xq = torch.empty((Mx, Kx), dtype=torch.uint8, device=dev)
+        sx = torch.empty((Kx // 128, Mx), dtype=torch.float32, device=dev)
+        xqT = torch.empty((Kx, Mx), dtype=torch.uint8, device=dev)
+        sxT = torch.empty((Mx // 128, Kx), dtype=torch.float32, device=dev)
+        dyq = torch.empty((Mx, Nw), dtype=torch.uint8, device=dev)
+        sdy = torch.empty((Nw // 128, Mx), dtype=torch.float32, device=dev)
+        dyqT = torch.empty((Nw, Mx), dtype=torch.uint8, device=dev)
+        sdyT = torch.empty((Mx // 128, Nw), dtype=torch.float32, device=dev)
+        y = torch.empty((Mx, Nw), dtype=torch.bfloat16, device=dev)
+        dx = torch.empty((Mx, Kx), dtype=torch.bfloat16, device=dev)
+        dw = torch.empty((Nw, Kx), dtype=torch.float32, device=dev)
+        f = 2.0 * Mx * Nw * Kx
+        parts = [
+            Part("quant_w_128x128", "quant_blocks_kernel", lambda: fg.fp8_quant_128x128(w, q=wq, scales=sw),
+                 "hbm", Q128X128_B * Nw * Kx),
+            Part("quant_x_1x128", "quant_rows_kernel", lambda: fg.fp8_quant_1x128(x, q=xq, scales=sx),
+                 "hbm", Q1X128_B * Mx * Kx),
+            Part("quant_x_transposed", "quant_cols_t_kernel",
+                 lambda: fg.fp8_quant_1x128(x, transpose=True, q=xqT, scales=sxT), "hbm", Q1X128_B * Mx * Kx),
+            Part("quant_dy_1x128", "quant_rows_kernel", lambda: fg.fp8_quant_1x128(dy, q=dyq, scales=sdy),
+                 "hbm", Q1X128_B * Mx * Nw),
+            Part("quant_dy_transposed", "quant_cols_t_kernel",
+                 lambda: fg.fp8_quant_1x128(dy, transpose=True, q=dyqT, scales=sdyT), "hbm", Q1X128_B * Mx * Nw),
+            Part("fprop", "gemm_kernel<FPROP>", lambda: fg.fprop(xq, sx, wq, sw, c=y), "tensor", f),
+            Part("dgrad", "gemm_kernel<DGRAD>", lambda: fg.dgrad(dyq, sdy, wq, sw, c=dx), "tensor", f),
+            Part("wgrad", "gemm_kernel<WGRAD>", lambda: fg.wgrad(dyqT, sdyT, xqT, sxT, c=dw), "tensor", f),
+        ]
+        W.update(inputs=[x, dy], outputs=[y, dx, dw], flops=3 * f, dims={"M": Mx, "K": Kx, "N": Nw})
+    elif workload == "moe":
+        mo = synth.moe(seed=seed, device=dev, make_weights=False)
+        E, Nw, Kx = 256, 2048, mo.x.shape[1]
+        # weights one expert at a time (bf16 for all 256 would be 7.5 GB)
+        wq = torch.empty((E, Nw, Kx), dtype=torch.uint8, device=dev)
+        sw = torch.empty((E, Nw // 128, Kx // 128), dtype=torch.float32, device=dev)
+        g = torch.Generator(device=dev)
+        g.manual_seed(seed + 1)
+        for e in range(E):
+            we = (torch.randn(Nw, Kx, generator=g, device=dev) * 0.02).to(torch.bfloat16)
+            fg.fp8_quant_128x128(we, q=wq[e], scales=sw[e])
+        T = mo.x.shape[0]
+        R = int(mo.expert_offsets[-1].item())
+        xq = torch.empty((T, Kx), dtype=torch.uint8, device=dev)
+        sx = torch.empty((Kx // 128, T), dtype=torch.float32, device=dev)
+        y = torch.empty((R, Nw), dtype=torch.bfloat16, device=dev)
+        nonempty = int((mo.counts > 0).sum().item())
+        moved = nonempty * Nw * Kx + R * Kx + R * Nw * 2 + sw.numel() * 4 + T * (Kx // 128) * 4
+        f = 2.0 * R * Nw * Kx
+        parts = [
+            Part("quant_x_1x128", "quant_rows_kernel", lambda: fg.fp8_quant_1x128(mo.x, q=xq, scales=sx), "hbm",
+                 Q1X128_B * T * Kx),
+            Part("grouped", "gemm_kernel<GROUPED>",
+                 lambda: fg.fp8_grouped_gemm(xq, sx, mo.row_index, mo.expert_offsets, wq, sw, R, y=y), "tensor",
+                 f, extra_bytes=moved),
+        ]
+        cnt = mo.counts.cpu()
+        W.update(inputs=[mo.x], outputs=[y], flops=f,
+                 dims={"tokens": T, "experts": E, "N": Nw, "K": Kx, "rows": R, "nonempty_experts": nonempty,
+                       "rows_per_expert_max": int(cnt.max()), "rows_per_expert_median": float(cnt.float().median())})
+    else:
+        raise ValueError(workload)
+    W["parts"] = parts
+    return W
+
+
+# ------------------------------------------------------------------ timing ----
+
+def kernel_source_sha():
+    h = hashlib.sha256()
+    for f in ("gemm.cu", "quant.cu", "ptx.cuh"):
+        with open(os.path.join(ROOT, "fp8_fine_grained_gb300", "csrc", f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def load_traffic(workload):
+    """DRAM bytes per launch from the committed ncu capture, or {} when the
+    kernel sources changed since the counters were taken."""
+    try:
+        with open(os.path.join(ROOT, "profiles", "traffic.json")) as f:
+            d = json.load(f)
+    except (OSError, ValueError):
+        return {}
+    if d.get("source_sha") != kernel_source_sha():
+        return {}
+    return d.get(workload, {})
 
 
 def run_ours(args):
@@ -121,97 +296,119 @@ def run_ours(args):
     pg = None
     if world > 1:
         import torch.distributed as dist
-        dist.init_process_group("nccl" if torch.cuda.is_available() else "gloo")
+        dist.init_process_group("nccl")
         pg = dist
 
-    x, w = synth.dense(seed=rank, device=dev, M=M, K=K, N=N)
-    wq, sw = fg.fp8_quant_128x128(w)
-    del w
-    xq = torch.empty((M, K), dtype=torch.uint8, device=dev)
-    sx = torch.empty((K // 128, M), dtype=torch.float32, device=dev)
-    y = torch.empty((M, N), dtype=torch.bfloat16, device=dev)
+    W = build(args.workload, dev, rank, fg, synth)
+    parts = W["parts"]
     flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
+    clean = torch.ones(L2_CLEAN_BYTES // 4, dtype=torch.float32, device=dev)
+    sink = torch.empty((), dtype=torch.float32, device=dev)
     stream = torch.cuda.current_stream()
 
-    def step():
-        fg.fp8_quant_1x128(x, q=xq, scales=sx)
-        fg.fprop(xq, sx, wq, sw, c=y)
+    def flush_l2():
+        flush.zero_()
+        torch.sum(clean, dim=0, out=sink)
 
     for _ in range(args.warmup):
-        step()
+        for p_ in parts:
+            p_.fn()
     torch.cuda.synchronize()
     if fg.device_status() != 0:
         raise RuntimeError("device status after warm-up")
 
-    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(args.steps)]
-    hbm, bf16_burst, bf16_sust, peak_kind = peaks()
-    clocks = ClockSampler(local, os.path.join(ROOT, "gpurun_out", "bench_clocks_rank%d.csv" % rank)
-                          if os.path.isdir(os.path.join(ROOT, "gpurun_out")) else "/tmp/fp8fg_clocks_%d.csv" % rank)
+    n = len(parts)
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(n + 1)] for _ in range(args.steps)]
+    hbm, bf16, peak_kind = peaks()
+    fp8_peak = 2.0 * bf16   # nominal FP8/BF16 dense ratio 4.5/2.25 on the measured BF16 burst
+    clk_path = os.path.join(ROOT, "gpurun_out", "bench_clocks_rank%d.csv" % rank) \
+        if os.path.isdir(os.path.join(ROOT, "gpurun_out")) else "/tmp/fp8fg_clocks_%d.csv" % rank
+    clocks = ClockSampler(local, clk_path)
     if pg:
         pg.barrier()
     torch.cuda.synchronize()
     with clocks:
         for i in range(args.steps):
-            flush.zero_()                       # evict L2 between steps (outside the events)
+            flush_l2()                           # outside the events
             ev[i][0].record(stream)
-            fg.fp8_quant_1x128(x, q=xq, scales=sx)
-            ev[i][1].record(stream)
-            fg.fprop(xq, sx, wq, sw, c=y)
-            ev[i][2].record(stream)
+            for j, p_ in enumerate(parts):
+                p_.fn()
+                ev[i][j + 1].record(stream)
         torch.cuda.synchronize()
     if pg:
         pg.barrier()
     if fg.device_status() != 0:
         raise RuntimeError("device status after timing")
-    t_quant = [ev[i][0].elapsed_time(ev[i][1]) for i in range(args.steps)]
-    t_gemm = [ev[i][1].elapsed_time(ev[i][2]) for i in range(args.steps)]
-    t_step = [a + b for a, b in zip(t_quant, t_gemm)]
-    ms_step = sum(t_step) / len(t_step)
-    ms_quant = sum(t_quant) / len(t_quant)
-    ms_gemm = sum(t_gemm) / len(t_gemm)
+    part_ms = [sum(ev[i][j].elapsed_time(ev[i][j + 1]) for i in range(args.steps)) / args.steps
+               for j in range(n)]
 
-    # end to end through the public API: pinned host X in, pinned host Y out
-    xh = x.cpu().pin_memory()
-    yh = torch.empty((M, N), dtype=torch.bfloat16).pin_memory()
-    xd = torch.empty_like(x)
+    # end to end through the public API: pinned host inputs in, pinned host outputs out
+    e2e = None
+    if args.workload in ("dense", "outliers", "tiny", "trio", "moe"):
+        hin = [t.cpu().pin_memory() for t in W["inputs"]]
+        hout = [torch.empty(t.shape, dtype=t.dtype).pin_memory() for t in W["outputs"]]
 
-    def e2e_step():
-        xd.copy_(xh, non_blocking=True)
-        fg.fp8_quant_1x128(xd, q=xq, scales=sx)
-        fg.fprop(xq, sx, wq, sw, c=y)
-        yh.copy_(y, non_blocking=True)
+        def e2e_step():
+            for d, h in zip(W["inputs"], hin):
+                d.copy_(h, non_blocking=True)
+            for p_ in parts:
+                p_.fn()
+            for d, h in zip(W["outputs"], hout):
+                h.copy_(d, non_blocking=True)
 
-    for _ in range(max(1, args.warmup)):
-        e2e_step()
-    torch.cuda.synchronize()
-    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    if pg:
-        pg.barrier()
-    e0.record(stream)
-    for _ in range(args.steps):
-        e2e_step()
-    e1.record(stream)
-    torch.cuda.synchronize()
-    ms_e2e = e0.elapsed_time(e1) / args.steps
+        for _ in range(max(1, args.warmup)):
+            e2e_step()
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e2e_steps = max(1, min(args.steps, 200))
+        if pg:
+            pg.barrier()
+        e0.record(stream)
+        for _ in range(e2e_steps):
+            e2e_step()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        e2e_ms = e0.elapsed_time(e1) / e2e_steps
+        e2e = {"ms": e2e_ms, "h2d": sum(t.numel() * t.element_size() for t in W["inputs"]),
+               "d2h": sum(t.numel() * t.element_size() for t in W["outputs"])}
 
-    if pg:
-        t = torch.tensor([ms_step, ms_e2e, ms_gemm, ms_quant], dtype=torch.float64, device=dev)
-        pg.all_reduce(t, op=pg.ReduceOp.MAX)
-        ms_step, ms_e2e, ms_gemm, ms_quant = [float(v) for v in t.tolist()]
-
-    flops = 2.0 * M * N * K
-    fp8_peak = 2.0 * bf16_burst           # nominal FP8/BF16 dense ratio 4.5/2.25 on the measured BF16 burst
-    gemm_tflops = flops / (ms_gemm * 1e-3) / 1e12
-    quant_gbs = QUANT_BYTES_PER_ELEM * M * K / (ms_quant * 1e-3) / 1e9
-    value = world * flops / (ms_step * 1e-3) / 1e12
-    e2e_value = world * flops / (ms_e2e * 1e-3) / 1e12
+    vals = reduce_max(part_ms + ([e2e["ms"]] if e2e else []), pg)
+    part_ms = vals[:n]
+    if e2e:
+        e2e["ms"] = vals[n]
+    ms_step = sum(part_ms)
+    value = world * W["flops"] / (ms_step * 1e-3) / 1e12
 
     if rank != 0:
         if pg:
             pg.destroy_process_group()
         return None
 
-    traffic = load_traffic()
+    traffic = load_traffic(args.workload)
+    kernels = []
+    for p_, ms in zip(parts, part_ms):
+        if p_.bound == "hbm":
+            ach, peak, unit = p_.units / (ms * 1e-3) / 1e9, hbm, "GB/s"
+        else:
+            ach, peak, unit = p_.units / (ms * 1e-3) / 1e12, fp8_peak, "TFLOP/s"
+        k = {"part": p_.name, "kernel": p_.kernel, "ms": round(ms, 4), "bound": p_.bound,
+             "achieved": round(ach, 1), "peak": round(peak, 1), "unit": unit, "frac": round(ach / peak, 4),
+             "traffic": traffic.get(p_.name)}
+        if p_.extra_bytes:
+            gbs = p_.extra_bytes / (ms * 1e-3) / 1e9
+            k["bytes"] = int(p_.extra_bytes)
+            k["achieved_gbs"] = round(gbs, 1)
+            k["frac_hbm"] = round(gbs / hbm, 4)
+        kernels.append(k)
+    dom = max(range(n), key=lambda j: part_ms[j])
+    dk = kernels[dom]
+    roofline = {"bound": dk["bound"], "kernel": dk["kernel"], "achieved": dk["achieved"], "peak": dk["peak"],
+                "unit": dk["unit"], "frac": dk["frac"], "traffic": dk["traffic"],
+                "peak_source": ("%s HBM copy" % peak_kind) if dk["bound"] == "hbm" else
+                ("%s bf16 burst %.0f TFLOP/s x 2 (nominal FP8/BF16 ratio)" % (peak_kind, bf16))}
+    if "frac_hbm" in dk:
+        roofline.update(achieved_gbs=dk["achieved_gbs"], frac_hbm=dk["frac_hbm"], hbm_peak=hbm)
+    quant = next((k for k in kernels if k["part"] == "quant_x_1x128"), None)
     line = {
         "metric": METRIC,
         "value": round(value, 2),
@@ -223,64 +420,48 @@ def run_ours(args):
         "higher_is_better": True,
         "scaling": "weak",
         "vs_baseline": None,
-        "dtype": "e4m3 x e4m3 -> f32 accumulate, bf16 out",
-        "data": "synthetic (seeded: X log-normal channels, W ~ N(0,0.02))",
-        "config": {"workload": WORKLOAD, "M": M, "K": K, "N": N, "l2": "flushed between steps (512 MiB write)",
-                   "weights": "pre-quantised 128x128 outside the timed region",
-                   "parallelism": "replica per GPU" if world > 1 else "single GPU"},
-        "roofline": {"bound": "tensor", "kernel": "gemm_kernel<FPROP,bf16>",
-                     "achieved": round(gemm_tflops, 1), "peak": round(fp8_peak, 1), "unit": "TFLOP/s",
-                     "frac": round(gemm_tflops / fp8_peak, 4),
-                     "peak_source": "%s bf16 burst %.0f TFLOP/s x 2 (nominal FP8/BF16 ratio)" % (peak_kind, bf16_burst),
-                     "traffic": traffic.get("gemm")},
-        "quant": {"kernel": "quant_rows_kernel", "ms": round(ms_quant, 4), "achieved": round(quant_gbs, 1),
-                  "peak": hbm, "unit": "GB/s", "frac": round(quant_gbs / hbm, 4), "bound": "hbm",
-                  "bytes_per_elem": QUANT_BYTES_PER_ELEM, "peak_source": peak_kind, "traffic": traffic.get("quant")},
-        "gemm_ms": round(ms_gemm, 4),
+        "dtype": "e4m3 x e4m3 -> f32 accumulate",
+        "data": "synthetic (seeded torch Philox; shapes and distributions of the workload)",
+        "config": dict({"workload": WORKLOADS[args.workload],
+                        "l2": "flushed between steps (512 MiB write + 256 MiB read, outside the timed region)",
+                        "parallelism": "replica per GPU" if world > 1 else "single GPU"}, **W["dims"]),
+        "roofline": roofline,
+        "quant": quant,
+        "kernels": kernels,
         "clocks": clocks.summary(),
-        "e2e": {"value": round(e2e_value, 2), "unit": "TFLOP/s", "h2d_bytes_per_step": M * K * 2,
-                "d2h_bytes_per_step": M * N * 2, "ms_per_step": round(ms_e2e, 4)},
-        "gpu_launches": 2 * args.steps,
+        "gpu_launches": n * args.steps,
     }
+    if e2e:
+        line["e2e"] = {"value": round(world * W["flops"] / (e2e["ms"] * 1e-3) / 1e12, 2), "unit": "TFLOP/s",
+                       "h2d_bytes_per_step": e2e["h2d"], "d2h_bytes_per_step": e2e["d2h"],
+                       "ms_per_step": round(e2e["ms"], 4)}
     if not args.no_cpu_baseline:
-        line["cpu_baseline"] = cpu_baseline(budget_s=args.cpu_seconds)
+        line["cpu_baseline"] = cpu_baseline(args.workload, budget_s=args.cpu_seconds)
     print(json.dumps(line), flush=True)
     if pg:
         pg.destroy_process_group()
     return line
 
 
-def kernel_source_sha():
-    import hashlib
-    h = hashlib.sha256()
-    for f in ("gemm.cu", "quant.cu", "ptx.cuh"):
-        with open(os.path.join(ROOT, "fp8_fine_grained_gb300", "csrc", f), "rb") as fh:
-            h.update(fh.read())
-    return h.hexdigest()[:16]
+# -------------------------------------------------------------- CPU oracle ----
+
+def oracle_dims(workload):
+    """(M, K, N) of the workload's first GEMM, the one the CPU sample runs."""
+    return {"dense": (4096, 7168, 7168), "outliers": (16384, 7168, 7168), "trio": (8192, 7168, 18432),
+            "moe": (32768, 7168, 2048), "tiny": (128, 256, 128)}[workload]
 
 
-def load_traffic():
-    """DRAM bytes per launch from the committed ncu capture, or {} when the
-    kernel sources changed since the counters were taken."""
-    path = os.path.join(ROOT, "profiles", "traffic.json")
-    try:
-        with open(path) as f:
-            d = json.load(f)
-    except (OSError, ValueError):
-        return {}
-    return d if d.get("source_sha") == kernel_source_sha() else {}
-
-
-def cpu_sample(rows, seed=0):
+def cpu_sample(workload, rows, seed=0):
     """Oracle on a bounded sample of the workload: 1x128 quantisation of
-    ``rows`` rows of X and their GEMM rows against the full pre-quantised W.
-    Returns (seconds, flops, threads)."""
-    import numpy as np
+    ``rows`` activation rows and their rows of the first GEMM against the
+    full pre-quantised weight. Returns (seconds, flops, threads)."""
     import torch
 
     import oracle
     from fp8_fine_grained_gb300 import synth
 
+    M, K, N = oracle_dims(workload)
+    rows = min(rows, M)
     g = torch.Generator()
     g.manual_seed(seed)
     c = torch.exp(torch.randn(K, generator=g))
@@ -295,28 +476,30 @@ def cpu_sample(rows, seed=0):
     return dt, 2.0 * rows * N * K, oracle.num_threads()
 
 
-def cpu_baseline(budget_s=15.0):
-    dt, fl, th = cpu_sample(8)
-    rows = max(8, min(4096, int(8 * budget_s / max(dt, 1e-3))))
-    dt, fl, th = cpu_sample(rows)
+def cpu_baseline(workload, budget_s=15.0):
+    M, K, N = oracle_dims(workload)
+    dt, fl, th = cpu_sample(workload, 8)
+    rows = max(8, min(M, int(8 * budget_s / max(dt, 1e-3))))
+    dt, fl, th = cpu_sample(workload, rows)
     return {"value": round(fl / dt / 1e12, 6), "unit": "TFLOP/s", "cores": th, "kind": "oracle",
-            "sample": "%d of %d rows of X quantised 1x128 and multiplied by the full 7168x7168 W "
-                      "(W quantised outside the timing); %.1f s" % (rows, M, dt)}
+            "sample": "%d of %d rows of X quantised 1x128 and multiplied by the full %dx%d W "
+                      "(W quantised outside the timing); %.1f s" % (rows, M, N, K, dt)}
 
 
 def run_reference(args):
     world, rank, local = dist_env()
     if rank != 0:
         return None
-    budget = max(1.0, min(20.0, args.cpu_seconds))
-    # size one step so that warmup + steps stay within a few minutes
-    dt, fl, th = cpu_sample(4)
-    rows = max(4, min(4096, int(4 * budget / max(dt, 1e-3))))
+    # keep the whole run (warm-up and timed steps) to about two minutes
+    budget = max(0.5, min(20.0, args.cpu_seconds, 120.0 / max(1, args.steps + args.warmup)))
+    M, K, N = oracle_dims(args.workload)
+    dt, fl, th = cpu_sample(args.workload, 4)
+    rows = max(4, min(M, int(4 * budget / max(dt, 1e-3))))
     for _ in range(args.warmup):
-        cpu_sample(min(rows, 8))
+        cpu_sample(args.workload, min(rows, 8))
     times = []
     for i in range(args.steps):
-        dt, fl, th = cpu_sample(rows, seed=i)
+        dt, fl, th = cpu_sample(args.workload, rows, seed=i)
         times.append(dt)
     ms = 1e3 * sum(times) / len(times)
     value = fl / (ms * 1e-3) / 1e12
@@ -325,7 +508,7 @@ def run_reference(args):
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms, 3), "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "e4m3 x e4m3 -> f64 block sums, f32 accumulate",
         "data": "synthetic (seeded)",
-        "config": {"workload": WORKLOAD, "M": M, "K": K, "N": N},
+        "config": {"workload": WORKLOADS[args.workload], "M": M, "K": K, "N": N},
         "cpu_baseline": {"value": round(value, 6), "unit": "TFLOP/s", "cores": th, "kind": "oracle",
                          "sample": "per step %d of %d rows of X, quantised and multiplied by the full W" % (rows, M)},
         "e2e": {"value": round(value, 6), "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
@@ -337,18 +520,24 @@ def run_reference(args):
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=20)
-    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--steps", type=int, default=None)
+    ap.add_argument("--warmup", type=int, default=None)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", choices=sorted(WORKLOADS), default="dense")
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args()
+    if args.impl == "reference":
+        args.steps = 3 if args.steps is None else args.steps
+        args.warmup = 1 if args.warmup is None else args.warmup
+        run_reference(args)
+        return
+    # the default timed region lasts about a second so that clock samples land in it
+    args.steps = 2000 if args.steps is None else args.steps
+    args.warmup = 20 if args.warmup is None else args.warmup
     if args.warmup < 3:
         args.warmup = 3
-    if args.impl == "reference":
-        run_reference(args)
-    else:
-        run_ours(args)
+    run_ours(args)
 
 
 if __name__ == "__main__":

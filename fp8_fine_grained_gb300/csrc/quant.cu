@@ -79,47 +79,50 @@ constexpr int QR_ROWS = 32;
 constexpr int QR_GROUPS = 4;
 constexpr int QR_ITEMS = QR_ROWS * QR_GROUPS / 16;
 
-__global__ void __launch_bounds__(256) quant_rows_kernel(const uint16_t *__restrict__ x, int64_t rows,
-                                                         int64_t ngroups, int64_t ldx, uint8_t *__restrict__ q,
-                                                         int64_t ldq, float *__restrict__ scales, int64_t ld_s)
+__global__ void __launch_bounds__(256, 4) quant_rows_kernel(const uint16_t *__restrict__ x, int64_t rows,
+                                                            int64_t ngroups, int64_t ldx, uint8_t *__restrict__ q,
+                                                            int64_t ldq, float *__restrict__ scales, int64_t ld_s)
 {
     __shared__ float s_scale[QR_GROUPS][QR_ROWS];
     const int hw = threadIdx.x >> 4;
     const int l = threadIdx.x & 15;
-    const int64_t r0 = (int64_t)blockIdx.x * QR_ROWS;
-    const int64_t g0 = (int64_t)blockIdx.y * QR_GROUPS;
+    // item i of this half-warp is row r0 + hw/4 + 4i, group g0 + hw%4: the
+    // group is fixed per thread and the row advances by 4 per item
+    const int rl = hw >> 2, gl = hw & 3;
+    const int64_t row0 = (int64_t)blockIdx.x * QR_ROWS + rl;
+    const int64_t g = (int64_t)blockIdx.y * QR_GROUPS + gl;
+    const bool g_ok = g < ngroups;
+    const uint16_t *src = x + row0 * ldx + g * GROUP + l * 8;
+    uint8_t *dst = q + row0 * ldq + g * GROUP + l * 8;
+    const int64_t rows_left = rows - row0;  // items with 4*i < rows_left are in range
 
     uint4 v[QR_ITEMS];
 #pragma unroll
     for (int i = 0; i < QR_ITEMS; ++i) {
-        const int t = i * 16 + hw;
-        const int64_t row = r0 + (t >> 2), g = g0 + (t & 3);
-        if (row < rows && g < ngroups)
-            v[i] = ld_stream_v4(x + row * ldx + g * GROUP + l * 8);
+        if (g_ok && 4 * i < rows_left)
+            v[i] = ld_stream_v4(src + (int64_t)(4 * i) * ldx);
         else
             v[i] = make_uint4(0, 0, 0, 0);
     }
 #pragma unroll
     for (int i = 0; i < QR_ITEMS; ++i) {
-        const int t = i * 16 + hw;
-        const int64_t row = r0 + (t >> 2), g = g0 + (t & 3);
         uint32_t m = absmax_bits8(v[i]);
 #pragma unroll
         for (int off = 8; off >= 1; off >>= 1)
             m = max(m, __shfl_xor_sync(0xffffffffu, m, off));
         const ScalePair sp = group_scale(__uint_as_float(m << 16));
-        if (row < rows && g < ngroups) {
-            *reinterpret_cast<uint2 *>(q + row * ldq + g * GROUP + l * 8) = quant8(v[i], sp.inv);
+        if (g_ok && 4 * i < rows_left) {
+            *reinterpret_cast<uint2 *>(dst + (int64_t)(4 * i) * ldq) = quant8(v[i], sp.inv);
             if (l == 0)
-                s_scale[t & 3][t >> 2] = sp.s;
+                s_scale[gl][rl + 4 * i] = sp.s;
         }
     }
     __syncthreads();
     if (threadIdx.x < QR_ROWS * QR_GROUPS) {
         const int gg = threadIdx.x / QR_ROWS, rr = threadIdx.x % QR_ROWS;
-        const int64_t row = r0 + rr, g = g0 + gg;
-        if (row < rows && g < ngroups)
-            scales[g * ld_s + row] = s_scale[gg][rr];
+        const int64_t row = (int64_t)blockIdx.x * QR_ROWS + rr, gs = (int64_t)blockIdx.y * QR_GROUPS + gg;
+        if (row < rows && gs < ngroups)
+            scales[gs * ld_s + row] = s_scale[gg][rr];
     }
 }
 

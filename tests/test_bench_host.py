@@ -1,0 +1,76 @@
+"""Host-side logic of bench.py (no GPU): clock-log parsing, the traffic
+lookup keyed by the kernel sources, and the max-over-ranks reduction run as
+two gloo ranks on the CPU."""
+import json
+import os
+
+import pytest
+import torch.multiprocessing as mp
+
+import bench
+
+
+def test_clock_summary_parses_nvidia_smi_csv(tmp_path):
+    p = tmp_path / "c.csv"
+    p.write_text("\n".join([
+        "2070, 2070, 900.5, 0x0, Not Active, Not Active, Not Active, Not Active",
+        "1950, 2070, 1390.0, 0x4, Not Active, Not Active, Not Active, Active",
+        "300, 2070, 200.0, 0x1, Not Active, Not Active, Not Active, Not Active",   # idle sample
+        "garbage line",
+    ]))
+    s = bench.summarize_clocks(str(p))
+    assert s["samples"] == 3
+    assert s["sm_max_mhz"] == 2070
+    assert s["sm_mhz"] == 2010.0          # median of the two loaded samples
+    assert s["reasons"] == ["sw_power_cap"]
+
+
+def test_clock_summary_without_samples(tmp_path):
+    s = bench.summarize_clocks(str(tmp_path / "missing.csv"))
+    assert s["samples"] == 0 and s["reasons"] == ["unsampled"]
+
+
+def test_traffic_lookup_follows_kernel_sources(tmp_path, monkeypatch):
+    prof = tmp_path / "profiles"
+    prof.mkdir()
+    (tmp_path / "fp8_fine_grained_gb300").mkdir()
+    (tmp_path / "fp8_fine_grained_gb300" / "csrc").symlink_to(os.path.join(bench.ROOT, "fp8_fine_grained_gb300", "csrc"))
+    monkeypatch.setattr(bench, "ROOT", str(tmp_path))
+    sha = bench.kernel_source_sha()
+    (prof / "traffic.json").write_text(json.dumps({"source_sha": sha, "dense": {"fprop": 123}}))
+    assert bench.load_traffic("dense") == {"fprop": 123}
+    (prof / "traffic.json").write_text(json.dumps({"source_sha": "0" * 16, "dense": {"fprop": 123}}))
+    assert bench.load_traffic("dense") == {}
+
+
+def test_workload_catalogue_matches_oracle_dims():
+    for w in bench.WORKLOADS:
+        M, K, N = bench.oracle_dims(w)
+        assert K % 128 == 0 and N % 128 == 0 and M > 0
+
+
+def _rank(rank, world, port, out):
+    import torch.distributed as dist
+    os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port), RANK=str(rank), WORLD_SIZE=str(world))
+    dist.init_process_group("gloo", rank=rank, world_size=world)
+    vals = bench.reduce_max([1.0 + rank, 10.0 - rank, 0.5 * rank], dist)
+    out[rank] = vals
+    dist.destroy_process_group()
+
+
+def test_reduce_max_over_two_gloo_ranks():
+    ctx = mp.get_context("spawn")
+    mgr = ctx.Manager()
+    out = mgr.dict()
+    port = 29500 + os.getpid() % 1000
+    procs = [ctx.Process(target=_rank, args=(r, 2, port, out)) for r in range(2)]
+    for p in procs:
+        p.start()
+    for p in procs:
+        p.join(120)
+        assert p.exitcode == 0
+    assert out[0] == out[1] == [2.0, 10.0, 0.5]
+
+
+def test_reduce_max_single_process_is_identity():
+    assert bench.reduce_max([3.0, 1.0], None) == [3.0, 1.0]
