@@ -58,11 +58,13 @@ constexpr uint32_t B_STAGE_BYTES = BN * BK;   // 32 KB
 constexpr uint32_t TMEM_COLS = 512;           // two 256-column partial buffers
 constexpr int MAX_EXPERTS = 4096;
 constexpr int MMA_K = 32;                     // K per tcgen05.mma for 8-bit operands
+constexpr int GATHER_WARPS = 2;               // grouped mode: warps 2..3 gather A rows
 
 enum Mode { FPROP = 0, DGRAD = 1, WGRAD = 2, GROUPED = 3 };
 
 struct Params {
     int64_t M, N, K;
+    const uint8_t *A;  // grouped mode: token rows gathered by cp.async
     const float *sA;
     int64_t ld_sA;
     const float *sB;
@@ -228,7 +230,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < STAGES; ++s) {
-            mbar_init(full_bar + 8 * s, 1);
+            mbar_init(full_bar + 8 * s, MODE == GROUPED ? 1 + GATHER_WARPS : 1);
             mbar_init(empty_bar + 8 * s, 1);
         }
         for (int b = 0; b < 2; ++b) {
@@ -264,19 +266,6 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         bool ok = true;
         for (int64_t t = blockIdx.x; t < num_tiles && ok; t += gridDim.x) {
             const Tile tl = decode_tile<MODE>(t, p, prefix);
-            int32_t tok[4] = {0, 0, 0, 0};
-            if constexpr (MODE == GROUPED) {
-#pragma unroll
-                for (int i = 0; i < 4; ++i) {
-                    const int64_t r = tl.m0 + lane * 4 + i;
-                    int32_t v = p.row_index[r < tl.row_end ? r : tl.m0];
-                    if (v < 0 || v >= p.n_tokens) {
-                        atomicCAS(p.status, 0, FP8FG_EDEVICE);
-                        v = 0;
-                    }
-                    tok[i] = v;
-                }
-            }
             for (int kb = 0; kb < num_kb; ++kb) {
                 bool got = true;
                 if (lane == 0)
@@ -292,7 +281,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 if (skip) {
                     skip = false;  // withhold this load: consumers must time out
                 } else {
-                    uint32_t bytes = A_STAGE_BYTES + B_STAGE_BYTES;
+                    // grouped: A rows arrive through the gather warps, not TMA
+                    uint32_t bytes = (MODE == GROUPED ? 0 : A_STAGE_BYTES) + B_STAGE_BYTES;
                     bool second_half = true;
                     if constexpr (MODE == DGRAD) {
                         second_half = tl.n0 + 128 < p.N;
@@ -306,7 +296,6 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                     }
                     __syncwarp();
                     if constexpr (MODE == GROUPED) {
-                        tma_gather4(a_dst + lane * 512, &tmA, kb * BK, tok[0], tok[1], tok[2], tok[3], fb);
                         if (lane == 0)
                             tma_load_2d(b_dst, &tmB, kb * BK, (int32_t)(tl.expert * p.N + tl.n0), fb);
                     } else if (lane == 0) {
@@ -538,6 +527,73 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 }
             }
         }
+    } else if constexpr (MODE == GROUPED) {
+        // ------------------------------------------------ row gather (A) ----
+        // Warps 2..3 copy the tile's 128 token rows, 128 bytes per row and
+        // contraction block, with 16-byte cp.async into the 128-byte
+        // swizzled layout TMA would produce (chunk c of row r at c ^ (r % 8)).
+        // Up to three blocks stay in flight per thread; when a block's copies
+        // have landed the thread fences them for the tensor cores' async
+        // proxy and the warp arrives on the stage's "full" barrier.
+        setmaxnreg_dec<LOW_REGS>();
+        const int gt = (warp - 2) * 32 + lane;  // rows 2*gt and 2*gt+1 of the tile
+        uint32_t stage = 0, phase = 0;
+        int64_t issued = 0, arrived = 0;          // blocks issued / blocks signalled
+        uint32_t arrive_stage = 0;
+        bool ok = true;
+        auto signal_oldest = [&]() {
+            fence_proxy_async_smem();
+            __syncwarp();
+            if (lane == 0)
+                mbar_arrive(full_bar + 8 * arrive_stage);
+            arrive_stage = arrive_stage + 1 == STAGES ? 0 : arrive_stage + 1;
+            ++arrived;
+        };
+        for (int64_t t = blockIdx.x; t < num_tiles && ok; t += gridDim.x) {
+            const Tile tl = decode_tile<MODE>(t, p, prefix);
+            const uint8_t *src[2];
+#pragma unroll
+            for (int j = 0; j < 2; ++j) {
+                const int64_t r = tl.m0 + 2 * gt + j;
+                int32_t v = p.row_index[r < tl.row_end ? r : tl.m0];
+                if (v < 0 || v >= p.n_tokens) {
+                    atomicCAS(p.status, 0, FP8FG_EDEVICE);
+                    v = 0;
+                }
+                src[j] = p.A + (int64_t)v * p.K;
+            }
+            for (int kb = 0; kb < num_kb; ++kb) {
+                bool got = true;
+                if (lane == 0)
+                    got = mbar_wait(empty_bar + 8 * stage, phase ^ 1, wc, FP8FG_ETIMEOUT);
+                got = __shfl_sync(0xffffffffu, got ? 1 : 0, 0) != 0;
+                if (!got) {
+                    ok = false;
+                    break;
+                }
+                const uint32_t a_dst = sbase + SmemLayout::a_off + stage * A_STAGE_BYTES;
+#pragma unroll
+                for (int j = 0; j < 2; ++j) {
+                    const int rr = 2 * gt + j;
+                    const uint8_t *s0 = src[j] + kb * BK;
+#pragma unroll
+                    for (int c = 0; c < 8; ++c)
+                        cp_async16(a_dst + rr * 128 + ((c ^ (rr & 7)) << 4), s0 + c * 16);
+                }
+                cp_async_commit();
+                ++issued;
+                cp_async_wait<2>();  // all but the two newest blocks have landed
+                while (arrived < issued - 2)
+                    signal_oldest();
+                if (++stage == STAGES) {
+                    stage = 0;
+                    phase ^= 1;
+                }
+            }
+        }
+        cp_async_wait<0>();
+        while (arrived < issued)
+            signal_oldest();
     } else {
         // warps 2..3 complete warpgroup 0 and have no role
         setmaxnreg_dec<LOW_REGS>();
@@ -750,7 +806,9 @@ extern "C" int fp8_grouped_gemm(const uint8_t *Xq, const float *sX, int64_t ld_s
     p.skip_first_load = 0;
 
     CUtensorMap ta, tb;
-    if (!make_map(&ta, Xq, (uint64_t)K, (uint64_t)n_tokens, (uint64_t)K, BK, 1))  // gather4: one-row box
+    p.A = Xq;
+    // A rows are gathered with cp.async; the A map is unused but kept valid
+    if (!make_map(&ta, Xq, (uint64_t)K, (uint64_t)n_tokens, (uint64_t)K, BK, 1))
         return FP8FG_ECUDA;
     if (!make_map(&tb, Wq, (uint64_t)K, (uint64_t)n_experts * (uint64_t)N, (uint64_t)K, BK, BN))
         return FP8FG_ECUDA;

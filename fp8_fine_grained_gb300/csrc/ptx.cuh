@@ -154,6 +154,30 @@ __device__ __forceinline__ uint64_t l2_policy_evict_first()
     return p;
 }
 
+// ------------------------------------------------------------- cp.async ----
+
+// 16-byte global -> shared copy through L2 only (no L1 allocation).
+__device__ __forceinline__ void cp_async16(uint32_t dst, const void *src)
+{
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
+}
+
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+
+// Wait until at most N of this thread's committed groups are still in flight.
+template <int N>
+__device__ __forceinline__ void cp_async_wait()
+{
+    asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
+}
+
+// Make this thread's completed shared-memory writes visible to later
+// async-proxy readers (TMA, tensor cores).
+__device__ __forceinline__ void fence_proxy_async_smem()
+{
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
 // -------------------------------------------------------------- tcgen05 ----
 
 // Allocate `ncols` tensor-memory columns (power of two, 32..512); the base
