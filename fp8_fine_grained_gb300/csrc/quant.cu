@@ -72,35 +72,37 @@ __device__ __forceinline__ uint4 ld_stream_v4(const void *p)
 }
 
 // ------------------------------------------------------ 1x128, per row ----
-// CTA tile: 32 rows x 4 groups (512 columns); 256 threads = 16 half-warps.
-// Item t = i*16 + half_warp (i = 0..7) is (row t/4, group t%4), so the two
-// half-warps of a warp read 512 contiguous bytes of one row per load.
-constexpr int QR_ROWS = 32;
-constexpr int QR_GROUPS = 4;
+// CTA tile: 4 rows x 16 groups (2048 columns); 256 threads = 16 half-warps.
+// Half-warp h owns group h of the tile and quantises it in each of the 4
+// rows, loading all four 256-byte segments before reducing any. The grid
+// walks the tiles in memory order (group blocks fastest). Small CTAs with
+// few registers keep eight per SM resident, which keeps enough loads in
+// flight to stream at HBM rate; a sweep of tile shapes on GB300 put this
+// one ahead of taller tiles with more loads per thread.
+constexpr int QR_ROWS = 4;
+constexpr int QR_GROUPS = 16;
 constexpr int QR_ITEMS = QR_ROWS * QR_GROUPS / 16;
 
-__global__ void __launch_bounds__(256, 4) quant_rows_kernel(const uint16_t *__restrict__ x, int64_t rows,
+__global__ void __launch_bounds__(256, 8) quant_rows_kernel(const uint16_t *__restrict__ x, int64_t rows,
                                                             int64_t ngroups, int64_t ldx, uint8_t *__restrict__ q,
-                                                            int64_t ldq, float *__restrict__ scales, int64_t ld_s)
+                                                            int64_t ldq, float *__restrict__ scales, int64_t ld_s,
+                                                            int64_t tiles_g)
 {
     __shared__ float s_scale[QR_GROUPS][QR_ROWS];
     const int hw = threadIdx.x >> 4;
     const int l = threadIdx.x & 15;
-    // item i of this half-warp is row r0 + hw/4 + 4i, group g0 + hw%4: the
-    // group is fixed per thread and the row advances by 4 per item
-    const int rl = hw >> 2, gl = hw & 3;
-    const int64_t row0 = (int64_t)blockIdx.x * QR_ROWS + rl;
-    const int64_t g = (int64_t)blockIdx.y * QR_GROUPS + gl;
+    const int64_t gb = blockIdx.x % tiles_g, rb = blockIdx.x / tiles_g;
+    const int64_t r0 = rb * QR_ROWS;
+    const int64_t g = gb * QR_GROUPS + hw;
     const bool g_ok = g < ngroups;
-    const uint16_t *src = x + row0 * ldx + g * GROUP + l * 8;
-    uint8_t *dst = q + row0 * ldq + g * GROUP + l * 8;
-    const int64_t rows_left = rows - row0;  // items with 4*i < rows_left are in range
+    const uint16_t *src = x + r0 * ldx + g * GROUP + l * 8;
+    uint8_t *dst = q + r0 * ldq + g * GROUP + l * 8;
 
     uint4 v[QR_ITEMS];
 #pragma unroll
     for (int i = 0; i < QR_ITEMS; ++i) {
-        if (g_ok && 4 * i < rows_left)
-            v[i] = ld_stream_v4(src + (int64_t)(4 * i) * ldx);
+        if (g_ok && r0 + i < rows)
+            v[i] = ld_stream_v4(src + (int64_t)i * ldx);
         else
             v[i] = make_uint4(0, 0, 0, 0);
     }
@@ -111,16 +113,16 @@ __global__ void __launch_bounds__(256, 4) quant_rows_kernel(const uint16_t *__re
         for (int off = 8; off >= 1; off >>= 1)
             m = max(m, __shfl_xor_sync(0xffffffffu, m, off));
         const ScalePair sp = group_scale(__uint_as_float(m << 16));
-        if (g_ok && 4 * i < rows_left) {
-            *reinterpret_cast<uint2 *>(dst + (int64_t)(4 * i) * ldq) = quant8(v[i], sp.inv);
+        if (g_ok && r0 + i < rows) {
+            *reinterpret_cast<uint2 *>(dst + (int64_t)i * ldq) = quant8(v[i], sp.inv);
             if (l == 0)
-                s_scale[gl][rl + 4 * i] = sp.s;
+                s_scale[hw][i] = sp.s;
         }
     }
     __syncthreads();
     if (threadIdx.x < QR_ROWS * QR_GROUPS) {
         const int gg = threadIdx.x / QR_ROWS, rr = threadIdx.x % QR_ROWS;
-        const int64_t row = (int64_t)blockIdx.x * QR_ROWS + rr, gs = (int64_t)blockIdx.y * QR_GROUPS + gg;
+        const int64_t row = r0 + rr, gs = gb * QR_GROUPS + gg;
         if (row < rows && gs < ngroups)
             scales[gs * ld_s + row] = s_scale[gg][rr];
     }
@@ -133,7 +135,7 @@ __global__ void __launch_bounds__(256, 4) quant_rows_kernel(const uint16_t *__re
 // the transposed output.
 constexpr int QT_COLS = 64;
 
-__global__ void __launch_bounds__(256) quant_cols_t_kernel(const uint16_t *__restrict__ x, int64_t rows,
+__global__ void __launch_bounds__(256, 8) quant_cols_t_kernel(const uint16_t *__restrict__ x, int64_t rows,
                                                            int64_t cols, int64_t ldx, uint8_t *__restrict__ qT,
                                                            int64_t ldq, float *__restrict__ scales, int64_t ld_s)
 {
@@ -259,11 +261,12 @@ extern "C" int fp8_quant_1x128(const void *x, int64_t rows, int64_t cols, int64_
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     if (transpose == 0) {
         const int64_t ngroups = cols / GROUP;
-        const int64_t gx = (rows + QR_ROWS - 1) / QR_ROWS, gy = (ngroups + QR_GROUPS - 1) / QR_GROUPS;
-        if (gx > 0x7FFFFFFF || gy > 65535)
+        const int64_t tiles_g = (ngroups + QR_GROUPS - 1) / QR_GROUPS;
+        const int64_t tiles = tiles_g * ((rows + QR_ROWS - 1) / QR_ROWS);
+        if (tiles > 0x7FFFFFFF)
             return FP8FG_EINVAL;
-        quant_rows_kernel<<<dim3((unsigned)gx, (unsigned)gy), 256, 0, s>>>(
-            static_cast<const uint16_t *>(x), rows, ngroups, ldx, q, ldq, scales, ld_s);
+        quant_rows_kernel<<<(unsigned)tiles, 256, 0, s>>>(static_cast<const uint16_t *>(x), rows, ngroups, ldx, q,
+                                                           ldq, scales, ld_s, tiles_g);
     } else {
         const int64_t gx = (cols + QT_COLS - 1) / QT_COLS, gy = rows / GROUP;
         if (gx > 0x7FFFFFFF || gy > 65535)
