@@ -59,6 +59,10 @@ constexpr uint32_t TMEM_COLS = 512;           // two 256-column partial buffers
 constexpr int MAX_EXPERTS = 4096;
 constexpr int MMA_K = 32;                     // K per tcgen05.mma for 8-bit operands
 constexpr int GATHER_WARPS = 2;               // grouped mode: warps 2..3 gather A rows
+// Epilogue staging: a promotion warp passes its 32 rows through a 2 KB
+// shared-memory block, 64 bytes of each row at a time, so that its global
+// stores cover 8 rows x 64 contiguous bytes each instead of 32 rows x 16.
+constexpr uint32_t STAGE_C_BYTES = 32 * 64;
 
 enum Mode { FPROP = 0, DGRAD = 1, WGRAD = 2, GROUPED = 3 };
 
@@ -95,9 +99,11 @@ struct SmemLayout {
     static constexpr uint32_t tmem_ptr_off = tempty_off + 8 * 2;
     static constexpr uint32_t abort_off = tmem_ptr_off + 4;
     static constexpr uint32_t misc_end = abort_off + 4;
-    static constexpr uint32_t wscale_off = (misc_end + 15) & ~15u;       // WGRAD column scales
-    static constexpr uint32_t wscale_end = wscale_off + EPI_WARPS * 128 * 4;
-    static constexpr uint32_t prefix_off = wscale_end;                    // GROUPED tile prefix
+    // per promotion warp: epilogue staging block; during the main loop its
+    // first 512 bytes hold the warp's 128 WGRAD column scales of the block
+    static constexpr uint32_t stage_c_off = (misc_end + 15) & ~15u;
+    static constexpr uint32_t stage_c_end = stage_c_off + EPI_WARPS * STAGE_C_BYTES;
+    static constexpr uint32_t prefix_off = stage_c_end;                   // GROUPED tile prefix
     static constexpr uint32_t prefix_end = prefix_off + 4 * (MAX_EXPERTS + 1);
     static constexpr uint32_t total = prefix_end + 1024;                 // + alignment slack
 };
@@ -397,7 +403,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         const int quarter = warp & 3;        // TMEM lanes 32*quarter .. +31
         const int half = ew >> 2;            // output columns half*128 .. +127 of the tile
         const int row_in_tile = quarter * 32 + lane;
-        float *wscale = reinterpret_cast<float *>(smem + SmemLayout::wscale_off) + ew * 128;
+        float *wscale = reinterpret_cast<float *>(smem + SmemLayout::stage_c_off + ew * STAGE_C_BYTES);
         uint32_t buf = 0, tphase = 0;
         bool ok = true;
         for (int64_t t = blockIdx.x; t < num_tiles && ok; t += gridDim.x) {
@@ -503,27 +509,59 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             }
             if (!ok)
                 break;
-            if (row_ok && cols_ok) {
-                if constexpr (OUT_BF16) {
-                    uint4 *dst = reinterpret_cast<uint4 *>(static_cast<__nv_bfloat16 *>(p.C) + row * p.ldc + col0);
+            if (!cols_ok)
+                continue;
+            // Round and store the warp's 32 rows x 128 columns, 64 bytes of
+            // each row per pass: each lane writes its row's piece into the
+            // staging block (16-byte piece c of row r at c ^ ((r / 2) % 4),
+            // conflict-free), then the warp reads it back 8 rows x 64 bytes
+            // per instruction and stores those runs. Rows past the tile's
+            // group (the next expert, or past M) are skipped.
+            {
+                constexpr int CW = OUT_BF16 ? 32 : 16;   // columns per 64-byte piece of a row
+                constexpr int ESZ = OUT_BF16 ? 2 : 4;
+                uint8_t *const stg = smem + SmemLayout::stage_c_off + ew * STAGE_C_BYTES;
+                // write side: this lane's row, pieces swizzled by (lane / 2) % 4
+                uint8_t *const w_row = stg + lane * 64;
+                const int w_sw = (lane >> 1) & 3;
+                // read side: row 8i + lane / 4, piece lane % 4 (the swizzle
+                // term of those rows does not depend on i)
+                const int cc = lane & 3;
+                const uint8_t *const r_ptr = stg + (lane >> 2) * 64 + ((cc ^ ((lane >> 3) & 3)) << 4);
+                const int rrow0 = row - lane + (lane >> 2);  // output row read back at i = 0
+                uint8_t *const out0 =
+                    static_cast<uint8_t *>(p.C) + ((int64_t)rrow0 * p.ldc + col0) * ESZ + cc * 16;
+                const int64_t row8 = 8 * p.ldc * ESZ;        // bytes between the rows of i and i + 1
 #pragma unroll
-                    for (int j = 0; j < 64; j += 4) {
+                for (int q = 0; q < 128 / CW; ++q) {
+#pragma unroll
+                    for (int c = 0; c < 4; ++c) {
                         uint4 o;
-                        __nv_bfloat162 h0 = __float22bfloat162_rn(acc[j + 0]);
-                        __nv_bfloat162 h1 = __float22bfloat162_rn(acc[j + 1]);
-                        __nv_bfloat162 h2 = __float22bfloat162_rn(acc[j + 2]);
-                        __nv_bfloat162 h3 = __float22bfloat162_rn(acc[j + 3]);
-                        o.x = *reinterpret_cast<uint32_t *>(&h0);
-                        o.y = *reinterpret_cast<uint32_t *>(&h1);
-                        o.z = *reinterpret_cast<uint32_t *>(&h2);
-                        o.w = *reinterpret_cast<uint32_t *>(&h3);
-                        dst[j / 4] = o;
+                        if constexpr (OUT_BF16) {
+                            const int a = q * 16 + c * 4;
+                            __nv_bfloat162 h0 = __float22bfloat162_rn(acc[a + 0]);
+                            __nv_bfloat162 h1 = __float22bfloat162_rn(acc[a + 1]);
+                            __nv_bfloat162 h2 = __float22bfloat162_rn(acc[a + 2]);
+                            __nv_bfloat162 h3 = __float22bfloat162_rn(acc[a + 3]);
+                            o.x = *reinterpret_cast<uint32_t *>(&h0);
+                            o.y = *reinterpret_cast<uint32_t *>(&h1);
+                            o.z = *reinterpret_cast<uint32_t *>(&h2);
+                            o.w = *reinterpret_cast<uint32_t *>(&h3);
+                        } else {
+                            const int a = q * 8 + c * 2;
+                            o = make_uint4(__float_as_uint(acc[a].x), __float_as_uint(acc[a].y),
+                                           __float_as_uint(acc[a + 1].x), __float_as_uint(acc[a + 1].y));
+                        }
+                        *reinterpret_cast<uint4 *>(w_row + ((c ^ w_sw) << 4)) = o;
                     }
-                } else {
-                    float4 *dst = reinterpret_cast<float4 *>(static_cast<float *>(p.C) + row * p.ldc + col0);
+                    __syncwarp();
 #pragma unroll
-                    for (int j = 0; j < 64; j += 2)
-                        dst[j / 2] = make_float4(acc[j].x, acc[j].y, acc[j + 1].x, acc[j + 1].y);
+                    for (int i = 0; i < 4; ++i) {
+                        const uint4 v = *reinterpret_cast<const uint4 *>(r_ptr + i * 512);
+                        if (rrow0 + 8 * i < tl.row_end)
+                            *reinterpret_cast<uint4 *>(out0 + i * row8 + q * 64) = v;
+                    }
+                    __syncwarp();
                 }
             }
         }
