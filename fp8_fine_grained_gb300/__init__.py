@@ -42,6 +42,7 @@ def lib():
         L = ctypes.CDLL(LIB_PATH)
         P, I64, I32 = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int
         L.fp8_quant_1x128.argtypes = [P, I64, I64, I64, P, I64, P, I64, I32, P]
+        L.fp8_quant_1x128_gather.argtypes = [P, I64, I64, I64, P, I64, P, I64, P, I64, P]
         L.fp8_quant_128x128.argtypes = [P, I64, I64, I64, P, I64, P, P]
         L.fp8_gemm_blockscaled.argtypes = [I32, P, P, I64, I64, P, P, I64, I64, I64, I64, I64, P, I32, I64, P]
         L.fp8_grouped_gemm.argtypes = [P, P, I64, I64, P, P, ctypes.c_int32, I64, P, P, I64, I64, P, I32, I64, P]
@@ -125,6 +126,29 @@ def fp8_quant_1x128(x, transpose=False, q=None, scales=None, stream=None):
     return q, scales
 
 
+def fp8_quant_1x128_gather(x, row_index, q=None, scales=None, stream=None):
+    """1x128 quantisation of the rows x[row_index[r]], written in row_index
+    order (MoE rows grouped by expert): q uint8 [n_rows, cols], scales
+    float32 [cols/128, ld_s>=n_rows]. Equal to gathering the rows of
+    fp8_quant_1x128(x); feeds fp8_grouped_gemm with row_index=None."""
+    torch = _torch()
+    _rowmajor(x, "x")
+    if x.dtype != torch.bfloat16:
+        raise ValueError("x must be bfloat16")
+    if row_index.dtype != torch.int32 or not row_index.is_contiguous():
+        raise ValueError("row_index must be contiguous int32")
+    n_src, cols = x.shape
+    rows = row_index.numel()
+    if q is None:
+        q = torch.empty((rows, cols), dtype=torch.uint8, device=x.device)
+    if scales is None:
+        scales = torch.empty((cols // 128, _pad(max(rows, 1), 4)), dtype=torch.float32, device=x.device)
+    rc = lib().fp8_quant_1x128_gather(_ptr(x), n_src, cols, x.stride(0), _ptr(row_index), rows, _ptr(q),
+                                      q.stride(0), _ptr(scales), scales.stride(0), _stream(stream))
+    _check(rc, "fp8_quant_1x128_gather")
+    return q, scales
+
+
 def fp8_quant_128x128(w, q=None, scales=None, stream=None):
     """E4M3 codes and FP32 scales of a bf16 weight [N, K] in 128x128 blocks.
     A 3-D weight [E, N, K] (MoE experts) is quantised as [E*N, K]."""
@@ -202,14 +226,16 @@ def fp8_grouped_gemm(xq, sx, row_index, expert_offsets, wq, sw, n_rows, out_dtyp
 
     xq [T, K] uint8, sx [K/128, >=T]; row_index int32 [n_rows]; expert_offsets
     int32 [E+1]; wq uint8 [E, N, K]; sw float32 [E, N/128, K/128].
+    row_index=None: xq/sx already hold the rows in expert order (for example
+    from fp8_quant_1x128_gather), row r of xq feeds output row r (T >= n_rows).
     """
     torch = _torch()
     _rowmajor(xq, "xq")
     _rowmajor(sx, "sx")
-    if row_index.dtype != torch.int32 or expert_offsets.dtype != torch.int32:
+    if expert_offsets.dtype != torch.int32 or (row_index is not None and row_index.dtype != torch.int32):
         raise ValueError("row_index and expert_offsets must be int32")
-    if not (row_index.is_contiguous() and expert_offsets.is_contiguous() and wq.is_contiguous()
-            and sw.is_contiguous()):
+    if not ((row_index is None or row_index.is_contiguous()) and expert_offsets.is_contiguous()
+            and wq.is_contiguous() and sw.is_contiguous()):
         raise ValueError("row_index, expert_offsets, wq, sw must be contiguous")
     T, K = xq.shape
     E, N, K2 = wq.shape
@@ -220,7 +246,8 @@ def fp8_grouped_gemm(xq, sx, row_index, expert_offsets, wq, sw, n_rows, out_dtyp
     if y is None:
         y = torch.empty((n_rows, N), dtype=out_dtype, device=xq.device)
     _rowmajor(y, "y")
-    rc = lib().fp8_grouped_gemm(_ptr(xq), _ptr(sx), sx.stride(0), T, _ptr(row_index), _ptr(expert_offsets), E,
+    ri = None if row_index is None else _ptr(row_index)
+    rc = lib().fp8_grouped_gemm(_ptr(xq), _ptr(sx), sx.stride(0), T, ri, _ptr(expert_offsets), E,
                                 n_rows, _ptr(wq), _ptr(sw), N, K, _ptr(y), _out_code(y.dtype), y.stride(0),
                                 _stream(stream))
     _check(rc, "fp8_grouped_gemm")

@@ -50,7 +50,7 @@ constexpr int CHUNK = 32;                     // TMEM columns per tcgen05.ld in 
 // per thread plus two 32-column partial buffers. The launch holds
 // NUM_THREADS x (compiled register count) registers; the split must fit in
 // it, which the host checks before every launch.
-constexpr int LOW_REGS = 40;
+constexpr int LOW_REGS = 56;
 constexpr int EPI_REGS = 224;
 constexpr int LAUNCH_REGS_MIN = (4 * 32 * LOW_REGS + EPI_WARPS * 32 * EPI_REGS + NUM_THREADS - 1) / NUM_THREADS;
 constexpr uint32_t A_STAGE_BYTES = BM * BK;   // 16 KB
@@ -103,7 +103,9 @@ struct SmemLayout {
     // first 512 bytes hold the warp's 128 WGRAD column scales of the block
     static constexpr uint32_t stage_c_off = (misc_end + 15) & ~15u;
     static constexpr uint32_t stage_c_end = stage_c_off + EPI_WARPS * STAGE_C_BYTES;
-    static constexpr uint32_t prefix_off = stage_c_end;                   // GROUPED tile prefix
+    static constexpr uint32_t tok_off = stage_c_end;                      // GROUPED: the tile's token rows
+    static constexpr uint32_t tok_end = tok_off + 4 * BM;
+    static constexpr uint32_t prefix_off = tok_end;                       // GROUPED tile prefix
     static constexpr uint32_t prefix_end = prefix_off + 4 * (MAX_EXPERTS + 1);
     static constexpr uint32_t total = prefix_end + 1024;                 // + alignment slack
 };
@@ -233,10 +235,13 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
     const WaitCtl wc{abort_flag, p.status, p.wait_limit_ns};
+    // grouped mode: A rows gathered through row_index by warps 2..3, or (no
+    // row index) already in expert order and loaded by TMA like the dense modes
+    const bool gathered = MODE == GROUPED && p.row_index != nullptr;
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < STAGES; ++s) {
-            mbar_init(full_bar + 8 * s, MODE == GROUPED ? 1 + GATHER_WARPS : 1);
+            mbar_init(full_bar + 8 * s, gathered ? 1 + GATHER_WARPS : 1);
             mbar_init(empty_bar + 8 * s, 1);
         }
         for (int b = 0; b < 2; ++b) {
@@ -287,8 +292,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 if (skip) {
                     skip = false;  // withhold this load: consumers must time out
                 } else {
-                    // grouped: A rows arrive through the gather warps, not TMA
-                    uint32_t bytes = (MODE == GROUPED ? 0 : A_STAGE_BYTES) + B_STAGE_BYTES;
+                    // gathered rows arrive through the gather warps, not TMA
+                    uint32_t bytes = (gathered ? 0 : A_STAGE_BYTES) + B_STAGE_BYTES;
                     bool second_half = true;
                     if constexpr (MODE == DGRAD) {
                         second_half = tl.n0 + 128 < p.N;
@@ -302,8 +307,11 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                     }
                     __syncwarp();
                     if constexpr (MODE == GROUPED) {
-                        if (lane == 0)
+                        if (lane == 0) {
+                            if (!gathered)
+                                tma_load_2d(a_dst, &tmA, kb * BK, (int32_t)tl.m0, fb);
                             tma_load_2d(b_dst, &tmB, kb * BK, (int32_t)(tl.expert * p.N + tl.n0), fb);
+                        }
                     } else if (lane == 0) {
                         tma_load_2d(a_dst, &tmA, kb * BK, (int32_t)tl.m0, fb);
                         if constexpr (MODE == DGRAD) {
@@ -413,7 +421,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             const int64_t col0 = tl.n0 + half * 128;
             const bool cols_ok = col0 < p.N;
             int64_t arow = row;  // row of the scale array sA
-            if constexpr (MODE == GROUPED) {
+            if (gathered) {
                 int32_t v = row_ok ? p.row_index[row] : 0;
                 arow = (v < 0 || v >= p.n_tokens) ? 0 : v;
             }
@@ -565,16 +573,23 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 }
             }
         }
-    } else if constexpr (MODE == GROUPED) {
+    } else if (gathered) {
         // ------------------------------------------------ row gather (A) ----
-        // Warps 2..3 copy the tile's 128 token rows, 128 bytes per row and
+        // Warps 2..3 copy the tile's token rows, 128 bytes per row and
         // contraction block, with 16-byte cp.async into the 128-byte
         // swizzled layout TMA would produce (chunk c of row r at c ^ (r % 8)).
-        // Up to three blocks stay in flight per thread; when a block's copies
-        // have landed the thread fences them for the tensor cores' async
-        // proxy and the warp arrives on the stage's "full" barrier.
+        // Warp w owns tile rows 64(w-2) .. +63; one instruction copies 4 whole
+        // rows (8 lanes per row), so each request is a full 128-byte line.
+        // The tile's token indices sit in shared memory; rows past the
+        // expert's end are not copied (their outputs are never stored, and an
+        // MMA row depends on its own A row only). Up to three blocks stay in
+        // flight; when a block's copies have landed the warp fences them for
+        // the tensor cores' async proxy and arrives on the stage's "full"
+        // barrier.
         setmaxnreg_dec<LOW_REGS>();
-        const int gt = (warp - 2) * 32 + lane;  // rows 2*gt and 2*gt+1 of the tile
+        const int wrow = (warp - 2) * 64;          // first tile row of this warp
+        const int chunk = lane & 7;                // 16-byte chunk of the row
+        int32_t *tok = reinterpret_cast<int32_t *>(smem + SmemLayout::tok_off);
         uint32_t stage = 0, phase = 0;
         int64_t issued = 0, arrived = 0;          // blocks issued / blocks signalled
         uint32_t arrive_stage = 0;
@@ -589,17 +604,21 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         };
         for (int64_t t = blockIdx.x; t < num_tiles && ok; t += gridDim.x) {
             const Tile tl = decode_tile<MODE>(t, p, prefix);
-            const uint8_t *src[2];
+            const int64_t left = tl.row_end - tl.m0;
+            const int nvalid = left < BM ? (int)left : BM;  // valid rows of the tile
 #pragma unroll
             for (int j = 0; j < 2; ++j) {
-                const int64_t r = tl.m0 + 2 * gt + j;
-                int32_t v = p.row_index[r < tl.row_end ? r : tl.m0];
-                if (v < 0 || v >= p.n_tokens) {
-                    atomicCAS(p.status, 0, FP8FG_EDEVICE);
-                    v = 0;
+                const int rr = wrow + 32 * j + lane;
+                if (rr < nvalid) {
+                    int32_t v = p.row_index[tl.m0 + rr];
+                    if (v < 0 || v >= p.n_tokens) {
+                        atomicCAS(p.status, 0, FP8FG_EDEVICE);
+                        v = 0;
+                    }
+                    tok[rr] = v;
                 }
-                src[j] = p.A + (int64_t)v * p.K;
             }
+            __syncwarp();
             for (int kb = 0; kb < num_kb; ++kb) {
                 bool got = true;
                 if (lane == 0)
@@ -610,13 +629,12 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                     break;
                 }
                 const uint32_t a_dst = sbase + SmemLayout::a_off + stage * A_STAGE_BYTES;
+                const uint8_t *a_src = p.A + (int64_t)kb * BK + chunk * 16;
 #pragma unroll
-                for (int j = 0; j < 2; ++j) {
-                    const int rr = 2 * gt + j;
-                    const uint8_t *s0 = src[j] + kb * BK;
-#pragma unroll
-                    for (int c = 0; c < 8; ++c)
-                        cp_async16(a_dst + rr * 128 + ((c ^ (rr & 7)) << 4), s0 + c * 16);
+                for (int i = 0; i < 16; ++i) {
+                    const int rr = wrow + 4 * i + (lane >> 3);
+                    if (rr < nvalid)
+                        cp_async16(a_dst + rr * 128 + ((chunk ^ (rr & 7)) << 4), a_src + (int64_t)tok[rr] * p.K);
                 }
                 cp_async_commit();
                 ++issued;
@@ -628,6 +646,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                     phase ^= 1;
                 }
             }
+            __syncwarp();  // every lane has read this tile's token rows
         }
         cp_async_wait<0>();
         while (arrived < issued)
@@ -814,7 +833,9 @@ extern "C" int fp8_grouped_gemm(const uint8_t *Xq, const float *sX, int64_t ld_s
         // nothing can be written; offsets are not inspected
         return FP8FG_OK;
     }
-    if (!Xq || !sX || !row_index || !Wq || !sW || !Y)
+    if (!Xq || !sX || !Wq || !sW || !Y)
+        return FP8FG_EINVAL;
+    if (!row_index && n_tokens < n_rows)  // rows already in expert order: row r is Xq row r
         return FP8FG_EINVAL;
     if (!aligned16(Xq) || !aligned16(Wq) || !aligned16(sX) || !aligned16(Y) || K % 16 != 0 || ld_sX % 4 != 0 ||
         (ldy * esz) % 16 != 0)
@@ -845,8 +866,9 @@ extern "C" int fp8_grouped_gemm(const uint8_t *Xq, const float *sX, int64_t ld_s
 
     CUtensorMap ta, tb;
     p.A = Xq;
-    // A rows are gathered with cp.async; the A map is unused but kept valid
-    if (!make_map(&ta, Xq, (uint64_t)K, (uint64_t)n_tokens, (uint64_t)K, BK, 1))
+    // with a row index the A rows are gathered with cp.async (the A map is
+    // then unused but kept valid); without one, TMA loads 128-row A tiles
+    if (!make_map(&ta, Xq, (uint64_t)K, (uint64_t)n_tokens, (uint64_t)K, BK, row_index ? 1 : BM))
         return FP8FG_ECUDA;
     if (!make_map(&tb, Wq, (uint64_t)K, (uint64_t)n_experts * (uint64_t)N, (uint64_t)K, BK, BN))
         return FP8FG_ECUDA;

@@ -83,10 +83,16 @@ constexpr int QR_ROWS = 4;
 constexpr int QR_GROUPS = 16;
 constexpr int QR_ITEMS = QR_ROWS * QR_GROUPS / 16;
 
+// GATHER: output row r quantises source row row_index[r] (rows listed in
+// MoE expert order); an index outside [0, n_src) is reported as
+// FP8FG_EDEVICE in the status word and reads source row 0. Quantisation is
+// per row, so the result equals gathering the rows of the plain output.
+template <bool GATHER>
 __global__ void __launch_bounds__(256, 8) quant_rows_kernel(const uint16_t *__restrict__ x, int64_t rows,
                                                             int64_t ngroups, int64_t ldx, uint8_t *__restrict__ q,
                                                             int64_t ldq, float *__restrict__ scales, int64_t ld_s,
-                                                            int64_t tiles_g)
+                                                            int64_t tiles_g, const int32_t *__restrict__ row_index,
+                                                            int64_t n_src, int *status)
 {
     __shared__ float s_scale[QR_GROUPS][QR_ROWS];
     const int hw = threadIdx.x >> 4;
@@ -101,10 +107,20 @@ __global__ void __launch_bounds__(256, 8) quant_rows_kernel(const uint16_t *__re
     uint4 v[QR_ITEMS];
 #pragma unroll
     for (int i = 0; i < QR_ITEMS; ++i) {
-        if (g_ok && r0 + i < rows)
-            v[i] = ld_stream_v4(src + (int64_t)i * ldx);
-        else
+        if (g_ok && r0 + i < rows) {
+            if constexpr (GATHER) {
+                int64_t sr = row_index[r0 + i];
+                if (sr < 0 || sr >= n_src) {
+                    atomicCAS(status, 0, FP8FG_EDEVICE);
+                    sr = 0;
+                }
+                v[i] = ld_stream_v4(x + sr * ldx + g * GROUP + l * 8);
+            } else {
+                v[i] = ld_stream_v4(src + (int64_t)i * ldx);
+            }
+        } else {
             v[i] = make_uint4(0, 0, 0, 0);
+        }
     }
 #pragma unroll
     for (int i = 0; i < QR_ITEMS; ++i) {
@@ -265,8 +281,9 @@ extern "C" int fp8_quant_1x128(const void *x, int64_t rows, int64_t cols, int64_
         const int64_t tiles = tiles_g * ((rows + QR_ROWS - 1) / QR_ROWS);
         if (tiles > 0x7FFFFFFF)
             return FP8FG_EINVAL;
-        quant_rows_kernel<<<(unsigned)tiles, 256, 0, s>>>(static_cast<const uint16_t *>(x), rows, ngroups, ldx, q,
-                                                           ldq, scales, ld_s, tiles_g);
+        quant_rows_kernel<false><<<(unsigned)tiles, 256, 0, s>>>(static_cast<const uint16_t *>(x), rows, ngroups,
+                                                                  ldx, q, ldq, scales, ld_s, tiles_g, nullptr, 0,
+                                                                  nullptr);
     } else {
         const int64_t gx = (cols + QT_COLS - 1) / QT_COLS, gy = rows / GROUP;
         if (gx > 0x7FFFFFFF || gy > 65535)
@@ -274,6 +291,34 @@ extern "C" int fp8_quant_1x128(const void *x, int64_t rows, int64_t cols, int64_
         quant_cols_t_kernel<<<dim3((unsigned)gx, (unsigned)gy), 256, 0, s>>>(
             static_cast<const uint16_t *>(x), rows, cols, ldx, q, ldq, scales, ld_s);
     }
+    return launch_status();
+}
+
+extern "C" int fp8_quant_1x128_gather(const void *x, int64_t n_src, int64_t cols, int64_t ldx,
+                                      const int32_t *row_index, int64_t rows, uint8_t *q, int64_t ldq, float *scales,
+                                      int64_t ld_s, void *stream)
+{
+    if (n_src < 0 || rows < 0 || cols < 0 || cols % GROUP != 0 || ldx < cols || ldq < cols || ld_s < rows)
+        return FP8FG_EINVAL;
+    if (rows == 0 || cols == 0)
+        return FP8FG_OK;
+    if (!x || !row_index || !q || !scales || n_src == 0)
+        return FP8FG_EINVAL;
+    if (!aligned16(x) || !aligned16(q) || !aligned16(scales) || ldx % 8 != 0 || ldq % 16 != 0 || ld_s % 4 != 0)
+        return FP8FG_EALIGN;
+    if (!device_supported())
+        return FP8FG_EUNSUPPORTED;
+    int *status = status_word_ptr();
+    if (!status)
+        return FP8FG_ECUDA;
+    const int64_t ngroups = cols / GROUP;
+    const int64_t tiles_g = (ngroups + QR_GROUPS - 1) / QR_GROUPS;
+    const int64_t tiles = tiles_g * ((rows + QR_ROWS - 1) / QR_ROWS);
+    if (tiles > 0x7FFFFFFF)
+        return FP8FG_EINVAL;
+    quant_rows_kernel<true><<<(unsigned)tiles, 256, 0, static_cast<cudaStream_t>(stream)>>>(
+        static_cast<const uint16_t *>(x), rows, ngroups, ldx, q, ldq, scales, ld_s, tiles_g, row_index, n_src,
+        status);
     return launch_status();
 }
 

@@ -107,6 +107,31 @@ FP8FG_API int fp8_quant_1x128(const void *x, int64_t rows, int64_t cols, int64_t
                     int transpose, void *stream);
 
 /* ---------------------------------------------------------------------
+ * fp8_quant_1x128_gather: 1x128 activation quantisation of selected rows,
+ * written in the order of a row index (MoE rows grouped by expert).
+ * Source: the 1x128 rule of fp8_quant_1x128 (innerforce.co.kr, fine-grained
+ * quantization paragraph); yunhecapital.com 2.2.2 (each token is routed to
+ * 8 of 256 experts). The tiles are per row, so the result is exactly the
+ * rows row_index[0..rows) of fp8_quant_1x128(x): the quantised tokens
+ * dispatched to their experts in one pass.
+ *
+ *   x         bf16 [n_src][ldx], ldx >= cols, cols % 128 == 0.
+ *   row_index int32 [rows], device: source row of output row r. Entries
+ *             outside [0, n_src) are reported as FP8FG_EDEVICE through
+ *             fp8fg_device_status and read source row 0.
+ *   q         E4M3 bytes [rows][ldq], ldq >= cols.
+ *   scales    FP32 [cols/128][ld_s], ld_s >= rows (the GEMM's layout).
+ *   Alignment: x, q, scales 16-byte aligned; ldx % 8 == 0, ldq % 16 == 0,
+ *   ld_s % 4 == 0. All buffers are owned by the caller; nothing is
+ *   allocated. rows == 0 or cols == 0 is a no-op; n_src == 0 with rows > 0
+ *   is FP8FG_EINVAL.
+ * ------------------------------------------------------------------- */
+FP8FG_API int fp8_quant_1x128_gather(const void *x, int64_t n_src, int64_t cols, int64_t ldx,
+                           const int32_t *row_index, int64_t rows,
+                           uint8_t *q, int64_t ldq, float *scales, int64_t ld_s,
+                           void *stream);
+
+/* ---------------------------------------------------------------------
  * fp8_quant_128x128: weight quantisation in 128x128 blocks.
  * Source: innerforce.co.kr, fine-grained quantization paragraph ("per 128
  * input channels per 128 output channels"); yunhecapital.com 2.2.3;
@@ -172,6 +197,10 @@ FP8FG_API int fp8_gemm_blockscaled(int mode,
  *   row_index int32 [n_rows], device: token of each row, rows grouped by
  *             expert. Entries outside [0, n_tokens) are reported as
  *             FP8FG_EDEVICE through fp8fg_device_status and read token 0.
+ *             NULL: Xq and sX already hold the rows in expert order (as
+ *             fp8_quant_1x128_gather writes them); output row r reads Xq
+ *             row r, and n_tokens >= n_rows is required (else EINVAL).
+ *             A tile's rows are then loaded by TMA instead of gathered.
  *   expert_offsets int32 [n_experts+1], device, non-decreasing, off[0] = 0,
  *             off[n_experts] <= n_rows. Rows at or beyond off[n_experts] are
  *             not written.

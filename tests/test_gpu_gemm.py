@@ -159,6 +159,32 @@ def test_grouped_small(out):
     check_gemm(to_np(y), c, t, out == "bf16", "grouped")
 
 
+@pytest.mark.parametrize("out", ["f32", "bf16"])
+def test_grouped_rows_in_expert_order(out):
+    """Without a row index: the rows are quantised straight into expert
+    order (fp8_quant_1x128_gather) and the GEMM loads 128-row A tiles with
+    TMA. Rows past the last offset stay untouched."""
+    x, w, row_index, off = _moe_small(seed=24)
+    R = int(off[-1])
+    ri = torch.from_numpy(row_index).to(DEV)
+    xg, sxg = fg.fp8_quant_1x128_gather(x, ri)
+    wq, sw = fg.fp8_quant_128x128(w)
+    dt = torch.float32 if out == "f32" else torch.bfloat16
+    y = torch.full((R + 40, w.shape[1]), 5.0, dtype=dt, device=DEV)
+    xg_pad = torch.zeros((R + 40, x.shape[1]), dtype=torch.uint8, device=DEV)
+    xg_pad[:R] = xg
+    sxg_pad = torch.zeros((sxg.shape[0], R + 40), dtype=torch.float32, device=DEV)
+    sxg_pad[:, :R] = sxg[:, :R]
+    fg.fp8_grouped_gemm(xg_pad, sxg_pad, None, torch.from_numpy(off).to(DEV), wq, sw, n_rows=R + 40, y=y)
+    assert fg.device_status() == 0
+    assert torch.all(y[R:] == 5.0)
+    xo, sxo = oracle.quant_1x128(bits(x))
+    assert np.array_equal(to_np(xg), xo[row_index])
+    wo, swo = to_np(wq), to_np(sw)
+    c, _, t = oracle.grouped(xo, sxo, row_index, off, wo, swo)
+    check_gemm(to_np(y[:R]), c, t, out == "bf16", "grouped, rows in expert order")
+
+
 def test_grouped_rows_beyond_last_offset_untouched():
     x, w, row_index, off = _moe_small(seed=22, counts=[3, 0, 130])
     xq, sx = fg.fp8_quant_1x128(x)

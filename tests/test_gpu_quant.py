@@ -6,7 +6,7 @@ import torch
 
 import oracle
 from fp8_fine_grained_gb300 import synth
-from tests.gpu_util import assert_quant_1x128, bits, to_np
+from tests.gpu_util import assert_quant_1x128, bits, rows_scales, to_np
 
 pytestmark = pytest.mark.gpu
 
@@ -108,6 +108,28 @@ def test_quant_dense_full_size():
     torch.cuda.synchronize()
     qo, so = oracle.quant_128x128(bits(w))
     assert np.array_equal(to_np(wq), qo) and np.array_equal(to_np(sw), so)
+
+
+@pytest.mark.parametrize("n_src,rows,cols", [(300, 1, 128), (300, 777, 384), (64, 1000, 7168)])
+def test_quant_1x128_gather(n_src, rows, cols):
+    """Rows quantised in row-index order (with repeats, as top-k routing
+    makes them) equal the oracle's 1x128 quantisation of those rows."""
+    x = _x(n_src, cols, seed=n_src + rows + cols)
+    ri = np.random.default_rng(rows).integers(0, n_src, rows).astype(np.int32)
+    q, s = fg.fp8_quant_1x128_gather(x, torch.from_numpy(ri).to(DEV))
+    assert fg.device_status() == 0
+    qo, so = oracle.quant_1x128(bits(x)[ri])
+    assert np.array_equal(to_np(q), qo)
+    assert np.array_equal(rows_scales(s, rows).view(np.uint32), so.view(np.uint32))
+
+
+def test_quant_1x128_gather_bad_index_reported():
+    x = _x(16, 256, seed=5)
+    ri = np.array([3, 10 ** 6, 0], np.int32)
+    q, s = fg.fp8_quant_1x128_gather(x, torch.from_numpy(ri).to(DEV))
+    assert fg.device_status() == 6  # FP8FG_EDEVICE; the bad row reads source row 0
+    qo, _ = oracle.quant_1x128(bits(x)[[3, 0, 0]])
+    assert np.array_equal(to_np(q), qo)
 
 
 def test_quant_zero_size_is_noop():
