@@ -159,12 +159,15 @@ def test_grouped_small(out):
     check_gemm(to_np(y), c, t, out == "bf16", "grouped")
 
 
-@pytest.mark.parametrize("out", ["f32", "bf16"])
-def test_grouped_rows_in_expert_order(out):
+@pytest.mark.parametrize("out,counts", [("f32", None), ("bf16", None),
+                                        ("bf16", [40, 64, 2, 65, 17, 33, 32, 0, 1]),
+                                        ("f32", [64, 63, 31, 129, 1])])
+def test_grouped_rows_in_expert_order(out, counts):
     """Without a row index: the rows are quantised straight into expert
     order (fp8_quant_1x128_gather) and the GEMM loads 128-row A tiles with
-    TMA. Rows past the last offset stay untouched."""
-    x, w, row_index, off = _moe_small(seed=24)
+    TMA, across expert sizes of 0..300 rows (tiles that straddle the next
+    expert's rows included). Rows past the last offset stay untouched."""
+    x, w, row_index, off = _moe_small(seed=24, counts=counts, E=9 if counts is None else len(counts))
     R = int(off[-1])
     ri = torch.from_numpy(row_index).to(DEV)
     xg, sxg = fg.fp8_quant_1x128_gather(x, ri)
@@ -173,7 +176,7 @@ def test_grouped_rows_in_expert_order(out):
     y = torch.full((R + 40, w.shape[1]), 5.0, dtype=dt, device=DEV)
     xg_pad = torch.zeros((R + 40, x.shape[1]), dtype=torch.uint8, device=DEV)
     xg_pad[:R] = xg
-    sxg_pad = torch.zeros((sxg.shape[0], R + 40), dtype=torch.float32, device=DEV)
+    sxg_pad = torch.zeros((sxg.shape[0], (R + 40 + 3) // 4 * 4), dtype=torch.float32, device=DEV)
     sxg_pad[:, :R] = sxg[:, :R]
     fg.fp8_grouped_gemm(xg_pad, sxg_pad, None, torch.from_numpy(off).to(DEV), wq, sw, n_rows=R + 40, y=y)
     assert fg.device_status() == 0
