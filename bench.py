@@ -12,7 +12,8 @@ inside the timed region.
 
 Other workloads, one JSON line each, for the remaining kernels:
     trio      linear layer 7168 -> 18432 at M = 8192: weight quantise, X and
-              dY quantised row-wise and transposed, fprop, dgrad, wgrad
+              dY quantised row-wise and transposed (both from one read),
+              fprop, dgrad, wgrad
     moe       4096 tokens, 256 experts (2048 x 7168), top-8 with a Zipf(1.1)
               expert bias: the routed rows of X quantised into expert order
               (1x128, one pass) + grouped expert GEMM
@@ -48,6 +49,7 @@ METRIC = "block-scaled FP8 GEMM TFLOP/s (% FP8 peak); quantize GB/s (% HBM)"
 L2_FLUSH_BYTES = 512 << 20
 L2_CLEAN_BYTES = 256 << 20
 Q1X128_B = 2 + 1 + 4.0 / 128       # bytes per element: read bf16, write E4M3, one FP32 scale per 128
+QDUAL_B = 2 + 2 * (1 + 4.0 / 128)  # one bf16 read, both layouts written
 Q128X128_B = 2 + 1 + 4.0 / 16384   # one FP32 scale per 128x128 block
 
 WORKLOADS = {
@@ -213,14 +215,14 @@ def build(workload, dev, seed, fg, synth):
         parts = [
             Part("quant_w_128x128", "quant_blocks_kernel", lambda: fg.fp8_quant_128x128(w, q=wq, scales=sw),
                  "hbm", Q128X128_B * Nw * Kx),
-            Part("quant_x_1x128", "quant_rows_kernel", lambda: fg.fp8_quant_1x128(x, q=xq, scales=sx),
-                 "hbm", Q1X128_B * Mx * Kx),
-            Part("quant_x_transposed", "quant_cols_t_kernel",
-                 lambda: fg.fp8_quant_1x128(x, transpose=True, q=xqT, scales=sxT), "hbm", Q1X128_B * Mx * Kx),
-            Part("quant_dy_1x128", "quant_rows_kernel", lambda: fg.fp8_quant_1x128(dy, q=dyq, scales=sdy),
-                 "hbm", Q1X128_B * Mx * Nw),
-            Part("quant_dy_transposed", "quant_cols_t_kernel",
-                 lambda: fg.fp8_quant_1x128(dy, transpose=True, q=dyqT, scales=sdyT), "hbm", Q1X128_B * Mx * Nw),
+            # X and dY each read once for both layouts (1x128 rows for
+            # fprop/dgrad, 128x1 transposed for wgrad)
+            Part("quant_x_dual", "quant_dual_kernel",
+                 lambda: fg.fp8_quant_1x128_dual(x, q=xq, scales=sx, qT=xqT, scalesT=sxT), "hbm",
+                 QDUAL_B * Mx * Kx),
+            Part("quant_dy_dual", "quant_dual_kernel",
+                 lambda: fg.fp8_quant_1x128_dual(dy, q=dyq, scales=sdy, qT=dyqT, scalesT=sdyT), "hbm",
+                 QDUAL_B * Mx * Nw),
             Part("fprop", "gemm_kernel<FPROP>", lambda: fg.fprop(xq, sx, wq, sw, c=y), "tensor", f),
             Part("dgrad", "gemm_kernel<DGRAD>", lambda: fg.dgrad(dyq, sdy, wq, sw, c=dx), "tensor", f),
             Part("wgrad", "gemm_kernel<WGRAD>", lambda: fg.wgrad(dyqT, sdyT, xqT, sxT, c=dw), "tensor", f),

@@ -43,6 +43,7 @@ def lib():
         P, I64, I32 = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int
         L.fp8_quant_1x128.argtypes = [P, I64, I64, I64, P, I64, P, I64, I32, P]
         L.fp8_quant_1x128_gather.argtypes = [P, I64, I64, I64, P, I64, P, I64, P, I64, P]
+        L.fp8_quant_1x128_dual.argtypes = [P, I64, I64, I64, P, I64, P, I64, P, I64, P, I64, P]
         L.fp8_quant_128x128.argtypes = [P, I64, I64, I64, P, I64, P, P]
         L.fp8_gemm_blockscaled.argtypes = [I32, P, P, I64, I64, P, P, I64, I64, I64, I64, I64, P, I32, I64, P]
         L.fp8_grouped_gemm.argtypes = [P, P, I64, I64, P, P, ctypes.c_int32, I64, P, P, I64, I64, P, I32, I64, P]
@@ -124,6 +125,31 @@ def fp8_quant_1x128(x, transpose=False, q=None, scales=None, stream=None):
                                scales.stride(0), 1 if transpose else 0, _stream(stream))
     _check(rc, "fp8_quant_1x128")
     return q, scales
+
+
+def fp8_quant_1x128_dual(x, q=None, scales=None, qT=None, scalesT=None, stream=None):
+    """Both layouts of fp8_quant_1x128 from one read of x (rows and cols
+    multiples of 128): returns (q, scales, qT, scalesT), equal to
+    fp8_quant_1x128(x) and fp8_quant_1x128(x, transpose=True)."""
+    torch = _torch()
+    _rowmajor(x, "x")
+    if x.dtype != torch.bfloat16:
+        raise ValueError("x must be bfloat16")
+    rows, cols = x.shape
+    dev = x.device
+    if q is None:
+        q = torch.empty((rows, cols), dtype=torch.uint8, device=dev)
+    if scales is None:
+        scales = torch.empty((cols // 128, _pad(max(rows, 1), 4)), dtype=torch.float32, device=dev)
+    if qT is None:
+        qT = torch.empty((cols, rows), dtype=torch.uint8, device=dev)
+    if scalesT is None:
+        scalesT = torch.empty((rows // 128, _pad(max(cols, 1), 4)), dtype=torch.float32, device=dev)
+    rc = lib().fp8_quant_1x128_dual(_ptr(x), rows, cols, x.stride(0), _ptr(q), q.stride(0), _ptr(scales),
+                                    scales.stride(0), _ptr(qT), qT.stride(0), _ptr(scalesT), scalesT.stride(0),
+                                    _stream(stream))
+    _check(rc, "fp8_quant_1x128_dual")
+    return q, scales, qT, scalesT
 
 
 def fp8_quant_1x128_gather(x, row_index, q=None, scales=None, stream=None):

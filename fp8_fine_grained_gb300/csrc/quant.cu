@@ -207,6 +207,80 @@ __global__ void __launch_bounds__(256, 8) quant_cols_t_kernel(const uint16_t *__
     }
 }
 
+// --------------------------------------- 1x128 and 128x1 from one read ----
+// Both activation layouts a training step needs (row groups for fprop and
+// dgrad, column groups transposed for wgrad) from a single read of x: the
+// CTA holds a 128x128 tile, quantises its rows straight from registers and
+// its columns from a shared-memory copy. The outputs are bit-identical to
+// fp8_quant_1x128 with transpose 0 and 1 (same group rule, same products).
+// 4.06 bytes of traffic per element instead of 2 x 3.03.
+__global__ void __launch_bounds__(256, 5) quant_dual_kernel(const uint16_t *__restrict__ x, int64_t ldx,
+                                                            uint8_t *__restrict__ q, int64_t ldq,
+                                                            float *__restrict__ scales, int64_t ld_s,
+                                                            uint8_t *__restrict__ qT, int64_t ldqT,
+                                                            float *__restrict__ scalesT, int64_t ld_sT)
+{
+    __shared__ __align__(16) uint16_t tile[GROUP][GROUP];
+    __shared__ uint32_t s_amax[2][GROUP];
+    __shared__ float s_row[GROUP];
+    const int tid = threadIdx.x;
+    const int l = tid & 15;
+    const int64_t c0 = (int64_t)blockIdx.x * GROUP;
+    const int64_t r0 = (int64_t)blockIdx.y * GROUP;
+
+    // chunk i*256 + tid = row (i*16 + tid/16), columns (tid%16)*8 .. +7
+    uint4 v[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i)
+        v[i] = ld_stream_v4(x + (r0 + i * 16 + (tid >> 4)) * ldx + c0 + l * 8);
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+        const int rr = i * 16 + (tid >> 4);
+        *reinterpret_cast<uint4 *>(&tile[rr][l * 8]) = v[i];
+        // row group: one half-warp per row
+        uint32_t m = absmax_bits8(v[i]);
+#pragma unroll
+        for (int off = 8; off >= 1; off >>= 1)
+            m = max(m, __shfl_xor_sync(0xffffffffu, m, off));
+        const ScalePair sp = group_scale(__uint_as_float(m << 16));
+        *reinterpret_cast<uint2 *>(q + (r0 + rr) * ldq + c0 + l * 8) = quant8(v[i], sp.inv);
+        if (l == 0)
+            s_row[rr] = sp.s;
+    }
+    __syncthreads();
+    if (tid < GROUP)
+        scales[(c0 / GROUP) * ld_s + r0 + tid] = s_row[tid];
+
+    // column groups: thread (c, part) covers rows part*64 .. +63 of column c
+    const int c = tid & (GROUP - 1), part = tid >> 7;
+    uint32_t m = 0;
+#pragma unroll 8
+    for (int i = 0; i < 64; ++i)
+        m = max(m, (uint32_t)(tile[part * 64 + i][c] & 0x7FFFu));
+    s_amax[part][c] = m;
+    __syncthreads();
+    m = max(s_amax[0][c], s_amax[1][c]);
+    const ScalePair sp = group_scale(__uint_as_float(m << 16));
+    const int64_t col = c0 + c;
+    uint4 *dst = reinterpret_cast<uint4 *>(qT + col * ldqT + r0 + part * 64);
+#pragma unroll
+    for (int h = 0; h < 4; ++h) {
+        uint32_t packed[4];
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            const int rb = part * 64 + h * 16 + j * 4;
+            const uint32_t lo = cvt_e4m3x2(__fmul_rn(__uint_as_float((uint32_t)tile[rb + 0][c] << 16), sp.inv),
+                                           __fmul_rn(__uint_as_float((uint32_t)tile[rb + 1][c] << 16), sp.inv));
+            const uint32_t hi = cvt_e4m3x2(__fmul_rn(__uint_as_float((uint32_t)tile[rb + 2][c] << 16), sp.inv),
+                                           __fmul_rn(__uint_as_float((uint32_t)tile[rb + 3][c] << 16), sp.inv));
+            packed[j] = lo | (hi << 16);
+        }
+        dst[h] = make_uint4(packed[0], packed[1], packed[2], packed[3]);
+    }
+    if (part == 0)
+        scalesT[(r0 / GROUP) * ld_sT + col] = sp.s;
+}
+
 // ------------------------------------------------------- 128x128 blocks ----
 // One CTA per block: 256 threads x 8 chunks of 8 bf16 held in registers.
 __global__ void __launch_bounds__(256) quant_blocks_kernel(const uint16_t *__restrict__ w, int64_t K, int64_t ldw,
@@ -319,6 +393,30 @@ extern "C" int fp8_quant_1x128_gather(const void *x, int64_t n_src, int64_t cols
     quant_rows_kernel<true><<<(unsigned)tiles, 256, 0, static_cast<cudaStream_t>(stream)>>>(
         static_cast<const uint16_t *>(x), rows, ngroups, ldx, q, ldq, scales, ld_s, tiles_g, row_index, n_src,
         status);
+    return launch_status();
+}
+
+extern "C" int fp8_quant_1x128_dual(const void *x, int64_t rows, int64_t cols, int64_t ldx, uint8_t *q,
+                                    int64_t ldq, float *scales, int64_t ld_s, uint8_t *qT, int64_t ldqT,
+                                    float *scalesT, int64_t ld_sT, void *stream)
+{
+    if (rows < 0 || cols < 0 || rows % GROUP != 0 || cols % GROUP != 0 || ldx < cols || ldq < cols || ld_s < rows ||
+        ldqT < rows || ld_sT < cols)
+        return FP8FG_EINVAL;
+    if (rows == 0 || cols == 0)
+        return FP8FG_OK;
+    if (!x || !q || !scales || !qT || !scalesT)
+        return FP8FG_EINVAL;
+    if (!aligned16(x) || !aligned16(q) || !aligned16(scales) || !aligned16(qT) || !aligned16(scalesT) ||
+        ldx % 8 != 0 || ldq % 16 != 0 || ldqT % 16 != 0 || ld_s % 4 != 0 || ld_sT % 4 != 0)
+        return FP8FG_EALIGN;
+    if (!device_supported())
+        return FP8FG_EUNSUPPORTED;
+    const int64_t gx = cols / GROUP, gy = rows / GROUP;
+    if (gx > 0x7FFFFFFF || gy > 65535)
+        return FP8FG_EINVAL;
+    quant_dual_kernel<<<dim3((unsigned)gx, (unsigned)gy), 256, 0, static_cast<cudaStream_t>(stream)>>>(
+        static_cast<const uint16_t *>(x), ldx, q, ldq, scales, ld_s, qT, ldqT, scalesT, ld_sT);
     return launch_status();
 }
 

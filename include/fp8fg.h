@@ -107,6 +107,31 @@ FP8FG_API int fp8_quant_1x128(const void *x, int64_t rows, int64_t cols, int64_t
                     int transpose, void *stream);
 
 /* ---------------------------------------------------------------------
+ * fp8_quant_1x128_dual: both activation layouts from one read of x.
+ * Source: the 1x128 rule of fp8_quant_1x128 (innerforce.co.kr, fine-grained
+ * quantization paragraph); tonho.wtf "o que isso custou" (the transposed read
+ * for the weight-gradient operands, and the wish to fuse the cast with the
+ * memory transfer).
+ *
+ * Writes exactly what fp8_quant_1x128(x, transpose = 0) and
+ * fp8_quant_1x128(x, transpose = 1) write, bit for bit, reading x once.
+ *   x       bf16 [rows][ldx], rows % 128 == 0, cols % 128 == 0, ldx >= cols.
+ *   q       E4M3 [rows][ldq] (ldq >= cols); scales FP32 [cols/128][ld_s],
+ *           ld_s >= rows: row r, group g at scales[g*ld_s + r].
+ *   qT      E4M3 [cols][ldqT] (ldqT >= rows): qT[c*ldqT + r]; scalesT FP32
+ *           [rows/128][ld_sT], ld_sT >= cols: column c, group g at
+ *           scalesT[g*ld_sT + c].
+ *   Alignment: x, q, scales, qT, scalesT 16-byte aligned; ldx % 8 == 0,
+ *   ldq % 16 == 0, ldqT % 16 == 0, ld_s % 4 == 0, ld_sT % 4 == 0.
+ *   All buffers belong to the caller; nothing is allocated. rows == 0 or
+ *   cols == 0 is a no-op.
+ * ------------------------------------------------------------------- */
+FP8FG_API int fp8_quant_1x128_dual(const void *x, int64_t rows, int64_t cols, int64_t ldx,
+                         uint8_t *q, int64_t ldq, float *scales, int64_t ld_s,
+                         uint8_t *qT, int64_t ldqT, float *scalesT, int64_t ld_sT,
+                         void *stream);
+
+/* ---------------------------------------------------------------------
  * fp8_quant_1x128_gather: 1x128 activation quantisation of selected rows,
  * written in the order of a row index (MoE rows grouped by expert).
  * Source: the 1x128 rule of fp8_quant_1x128 (innerforce.co.kr, fine-grained

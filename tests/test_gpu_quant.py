@@ -110,6 +110,32 @@ def test_quant_dense_full_size():
     assert np.array_equal(to_np(wq), qo) and np.array_equal(to_np(sw), so)
 
 
+@pytest.mark.parametrize("rows,cols", [(128, 128), (256, 384), (640, 1024), (1024, 7168)])
+def test_quant_dual(rows, cols):
+    """One read, both layouts: bit-identical to the oracle's 1x128 row
+    quantisation and its transposed 128x1 quantisation."""
+    x = _x(rows, cols, seed=rows + 3 * cols)
+    q, s, qT, sT = fg.fp8_quant_1x128_dual(x)
+    assert fg.device_status() == 0
+    assert_quant_1x128(x, q, s)
+    qo, so = oracle.quant_128x1_t(bits(x))
+    assert np.array_equal(to_np(qT), qo)
+    assert np.array_equal(to_np(sT)[:, :cols].view(np.uint32), so.view(np.uint32))
+
+
+def test_quant_dual_pitched_outputs():
+    base = _x(256, 640, seed=9)
+    x = base[:, :512]
+    q = torch.zeros((256, 528), dtype=torch.uint8, device=DEV)[:, :512]
+    qT = torch.zeros((512, 272), dtype=torch.uint8, device=DEV)[:, :256]
+    fg.fp8_quant_1x128_dual(x, q=q, qT=qT)
+    torch.cuda.synchronize()
+    qo, _ = oracle.quant_1x128(bits(x))
+    assert np.array_equal(to_np(q), qo)
+    qto, _ = oracle.quant_128x1_t(bits(x))
+    assert np.array_equal(to_np(qT), qto)
+
+
 @pytest.mark.parametrize("n_src,rows,cols", [(300, 1, 128), (300, 777, 384), (64, 1000, 7168)])
 def test_quant_1x128_gather(n_src, rows, cols):
     """Rows quantised in row-index order (with repeats, as top-k routing
