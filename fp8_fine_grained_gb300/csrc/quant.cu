@@ -62,6 +62,29 @@ __device__ __forceinline__ uint2 quant8(const uint4 &v, float inv)
     return o;
 }
 
+// Group scales of N groups per half-warp (N <= 16) with one division
+// sequence per warp: on entry every lane of half-warp h holds the amax bit
+// patterns m[0..N) of its N groups (shuffle-reduced over the half-warp);
+// lane (16h + j) computes the scale pair of group j and the pairs are
+// broadcast back. Bit-identical to calling group_scale per group.
+template <int N>
+__device__ __forceinline__ void group_scales_batched(const uint32_t (&m)[N], float (&s)[N], float (&inv)[N])
+{
+    static_assert(N <= 16, "one group per lane of a half-warp");
+    const int lane = threadIdx.x & 31;
+    const int j = lane & 15;
+    uint32_t mine = m[0];
+#pragma unroll
+    for (int i = 1; i < N; ++i)
+        mine = j == i ? m[i] : mine;
+    const ScalePair sp = group_scale(__uint_as_float(mine << 16));
+#pragma unroll
+    for (int i = 0; i < N; ++i) {
+        s[i] = __shfl_sync(0xffffffffu, sp.s, (lane & 16) + i);
+        inv[i] = __shfl_sync(0xffffffffu, sp.inv, (lane & 16) + i);
+    }
+}
+
 __device__ __forceinline__ uint4 ld_stream_v4(const void *p)
 {
     uint4 v;
@@ -122,17 +145,22 @@ __global__ void __launch_bounds__(256, 8) quant_rows_kernel(const uint16_t *__re
             v[i] = make_uint4(0, 0, 0, 0);
         }
     }
+    uint32_t m[QR_ITEMS];
 #pragma unroll
     for (int i = 0; i < QR_ITEMS; ++i) {
-        uint32_t m = absmax_bits8(v[i]);
+        m[i] = absmax_bits8(v[i]);
 #pragma unroll
         for (int off = 8; off >= 1; off >>= 1)
-            m = max(m, __shfl_xor_sync(0xffffffffu, m, off));
-        const ScalePair sp = group_scale(__uint_as_float(m << 16));
+            m[i] = max(m[i], __shfl_xor_sync(0xffffffffu, m[i], off));
+    }
+    float sc[QR_ITEMS], inv[QR_ITEMS];
+    group_scales_batched<QR_ITEMS>(m, sc, inv);
+#pragma unroll
+    for (int i = 0; i < QR_ITEMS; ++i) {
         if (g_ok && r0 + i < rows) {
-            *reinterpret_cast<uint2 *>(dst + (int64_t)i * ldq) = quant8(v[i], sp.inv);
+            *reinterpret_cast<uint2 *>(dst + (int64_t)i * ldq) = quant8(v[i], inv[i]);
             if (l == 0)
-                s_scale[hw][i] = sp.s;
+                s_scale[hw][i] = sc[i];
         }
     }
     __syncthreads();
@@ -233,19 +261,25 @@ __global__ void __launch_bounds__(256, 5) quant_dual_kernel(const uint16_t *__re
 #pragma unroll
     for (int i = 0; i < 8; ++i)
         v[i] = ld_stream_v4(x + (r0 + i * 16 + (tid >> 4)) * ldx + c0 + l * 8);
+    // row groups: one half-warp per row, the eight rows' scales in one batch
+    uint32_t mr[8];
 #pragma unroll
     for (int i = 0; i < 8; ++i) {
         const int rr = i * 16 + (tid >> 4);
         *reinterpret_cast<uint4 *>(&tile[rr][l * 8]) = v[i];
-        // row group: one half-warp per row
-        uint32_t m = absmax_bits8(v[i]);
+        mr[i] = absmax_bits8(v[i]);
 #pragma unroll
         for (int off = 8; off >= 1; off >>= 1)
-            m = max(m, __shfl_xor_sync(0xffffffffu, m, off));
-        const ScalePair sp = group_scale(__uint_as_float(m << 16));
-        *reinterpret_cast<uint2 *>(q + (r0 + rr) * ldq + c0 + l * 8) = quant8(v[i], sp.inv);
+            mr[i] = max(mr[i], __shfl_xor_sync(0xffffffffu, mr[i], off));
+    }
+    float sr[8], ir[8];
+    group_scales_batched<8>(mr, sr, ir);
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+        const int rr = i * 16 + (tid >> 4);
+        *reinterpret_cast<uint2 *>(q + (r0 + rr) * ldq + c0 + l * 8) = quant8(v[i], ir[i]);
         if (l == 0)
-            s_row[rr] = sp.s;
+            s_row[rr] = sr[i];
     }
     __syncthreads();
     if (tid < GROUP)
