@@ -17,15 +17,18 @@
 //               4 x tcgen05.mma (M128 N256 K32, E4M3 -> FP32) per block into
 //               one of two 256-column TMEM partial buffers, and commits to
 //               the stage's "empty" and the buffer's "full" barrier.
-//   warps 2..3  complete warpgroup 0 (no role) so that setmaxnreg can move
-//               its registers to the promotion warpgroups.
+//   warps 2..3  MoE experts with a row index: gather the tile's token rows
+//               into the A stage with cp.async; otherwise no role (they
+//               complete warpgroup 0 so that setmaxnreg can move its
+//               registers to the promotion warpgroups).
 //   warps 4..11 promotion/epilogue: each thread owns one output row and 128
 //               columns; per block it loads the partial from TMEM
 //               (tcgen05.ld 32x32b, 32 columns at a time, two loads in
 //               flight), does acc = fma(P, sA*sB, acc) in FP32 registers
 //               (paired FP32 FMAs) and frees the TMEM buffer, so the MMA of
 //               block kb+1 overlaps the promotion of block kb. After the
-//               last block it rounds and stores the row.
+//               last block it rounds its rows and stores them through a
+//               shared-memory staging block, 8 rows x 64 bytes per store.
 // Every wait is bounded (global timer); a wait that runs out records
 // FP8FG_ETIMEOUT in the device status word and all roles leave their loops,
 // drain their own in-flight copies and MMAs, and release tensor memory.

@@ -1,6 +1,7 @@
-// Fine-grained E4M3 quantisation kernels: 1x128 tiles (per row), 128x1 tiles
-// with transposed output (per column, for the weight-gradient operands), and
-// 128x128 blocks (weights).
+// Fine-grained E4M3 quantisation kernels: 1x128 tiles (per row, also for
+// rows gathered through a row index), 128x1 tiles with transposed output
+// (per column, for the weight-gradient operands), both of those from one
+// read, and 128x128 blocks (weights).
 //
 // Group rule (innerforce.co.kr, fine-grained quantization paragraph, Figure
 // 7(a); tonho.wtf DeepSeek-V3 entry, "como funciona"): amax = max |x| over
@@ -8,10 +9,11 @@
 // = 1 when amax is 0 or 448/amax overflows); code = E4M3(x*inv) with one FP32
 // product and one round-to-nearest-even, saturating conversion.
 //
-// All three kernels are HBM-bound streams (2 bytes read, 1 byte + 4/128 or
-// 4/16384 bytes written per element). They read with 16-byte vector loads
-// issued back to back (several in flight per thread), reduce the amax with
-// warp shuffles, and write codes and scales with full 32-byte sectors.
+// The kernels are streams bound by HBM and instruction issue (2 bytes read,
+// 1 byte + 4/128 or 4/16384 bytes written per element). They read with
+// 16-byte vector loads issued back to back (several in flight per thread),
+// reduce the amax with warp shuffles, and write codes and scales with full
+// 32-byte sectors.
 #include <cuda_bf16.h>
 
 #include "host_common.h"
