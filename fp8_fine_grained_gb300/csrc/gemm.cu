@@ -53,9 +53,13 @@ constexpr int CHUNK = 32;                     // TMEM columns per tcgen05.ld in 
 // per thread plus two 32-column partial buffers. The launch holds
 // NUM_THREADS x (compiled register count) registers; the split must fit in
 // it, which the host checks before every launch.
-constexpr int LOW_REGS = 56;
-constexpr int EPI_REGS = 224;
-constexpr int LAUNCH_REGS_MIN = (4 * 32 * LOW_REGS + EPI_WARPS * 32 * EPI_REGS + NUM_THREADS - 1) / NUM_THREADS;
+// The contiguous MoE mode (no gather warps, but a tile decode in every
+// role) moves 16 more registers to the promotion warps.
+template <int MODE> struct Regs {
+    static constexpr int LOW = MODE == 4 ? 40 : 56;
+    static constexpr int EPI = MODE == 4 ? 232 : 224;
+    static constexpr int LAUNCH_MIN = (4 * 32 * LOW + EPI_WARPS * 32 * EPI + NUM_THREADS - 1) / NUM_THREADS;
+};
 constexpr uint32_t A_STAGE_BYTES = BM * BK;   // 16 KB
 constexpr uint32_t B_STAGE_BYTES = BN * BK;   // 32 KB
 constexpr uint32_t TMEM_COLS = 512;           // two 256-column partial buffers
@@ -67,7 +71,11 @@ constexpr int GATHER_WARPS = 2;               // grouped mode: warps 2..3 gather
 // stores cover 8 rows x 64 contiguous bytes each instead of 32 rows x 16.
 constexpr uint32_t STAGE_C_BYTES = 32 * 64;
 
-enum Mode { FPROP = 0, DGRAD = 1, WGRAD = 2, GROUPED = 3 };
+// GROUPED: MoE experts, A rows gathered through a row index by warps 2..3.
+// GROUPED_C: MoE experts, A rows already in expert order (TMA tiles). Two
+// instantiations, so that neither carries the other's registers.
+enum Mode { FPROP = 0, DGRAD = 1, WGRAD = 2, GROUPED = 3, GROUPED_C = 4 };
+constexpr bool is_grouped(int mode) { return mode == GROUPED || mode == GROUPED_C; }
 
 struct Params {
     int64_t M, N, K;
@@ -130,7 +138,7 @@ template <int MODE>
 __device__ __forceinline__ Tile decode_tile(int64_t t, const Params &p, const int32_t *prefix)
 {
     Tile tl;
-    if constexpr (MODE == GROUPED) {
+    if constexpr (is_grouped(MODE)) {
         // experts are laid out in the tile space one after the other; within
         // an expert the m-tiles vary fastest, so CTAs running together share
         // the expert's weight tiles in L2.
@@ -238,9 +246,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
     const WaitCtl wc{abort_flag, p.status, p.wait_limit_ns};
-    // grouped mode: A rows gathered through row_index by warps 2..3, or (no
-    // row index) already in expert order and loaded by TMA like the dense modes
-    const bool gathered = MODE == GROUPED && p.row_index != nullptr;
+    // GROUPED: A rows gathered through row_index by warps 2..3; GROUPED_C:
+    // A rows already in expert order, loaded by TMA like the dense modes
+    constexpr bool gathered = MODE == GROUPED;
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < STAGES; ++s) {
@@ -260,7 +268,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         tmem_alloc(sbase + SmemLayout::tmem_ptr_off, TMEM_COLS);
         tmem_relinquish();
     }
-    if constexpr (MODE == GROUPED)
+    if constexpr (is_grouped(MODE))
         build_group_prefix(p, prefix);
     tc_fence_before();
     __syncthreads();
@@ -268,12 +276,12 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     const uint32_t tmem_base = *tmem_ptr;
 
     const int64_t num_tiles =
-        (MODE == GROUPED) ? (int64_t)grouped_total_tiles(prefix, p.n_experts) : p.num_m_tiles * p.num_n_tiles;
+        is_grouped(MODE) ? (int64_t)grouped_total_tiles(prefix, p.n_experts) : p.num_m_tiles * p.num_n_tiles;
     const int num_kb = (int)(p.K / BK);
 
     if (warp == 0) {
         // ------------------------------------------------------ producer ----
-        setmaxnreg_dec<LOW_REGS>();
+        setmaxnreg_dec<Regs<MODE>::LOW>();
         uint32_t stage = 0, phase = 0;
         uint32_t filled_mask = 0, fill_parity = 0;  // per stage: a fill was issued, and its parity
         bool skip = p.skip_first_load && blockIdx.x == 0;
@@ -309,7 +317,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                         fill_parity = (fill_parity & ~(1u << stage)) | (phase << stage);
                     }
                     __syncwarp();
-                    if constexpr (MODE == GROUPED) {
+                    if constexpr (is_grouped(MODE)) {
                         if (lane == 0) {
                             if (!gathered)
                                 tma_load_2d(a_dst, &tmA, kb * BK, (int32_t)tl.m0, fb);
@@ -348,7 +356,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         }
     } else if (warp == 1) {
         // ---------------------------------------------------------- MMA ----
-        setmaxnreg_dec<LOW_REGS>();
+        setmaxnreg_dec<Regs<MODE>::LOW>();
         if (lane == 0) {
             constexpr uint32_t IDESC = idesc_e4m3_f32(BM, BN, MODE == DGRAD);
             uint32_t stage = 0, phase = 0, buf = 0, tphase = 0;
@@ -409,7 +417,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         __syncwarp();
     } else if (warp >= EPI_WARP0) {
         // ------------------------------------------ promotion / epilogue ----
-        setmaxnreg_inc<EPI_REGS>();
+        setmaxnreg_inc<Regs<MODE>::EPI>();
         const int ew = warp - EPI_WARP0;
         const int quarter = warp & 3;        // TMEM lanes 32*quarter .. +31
         const int half = ew >> 2;            // output columns half*128 .. +127 of the tile
@@ -436,7 +444,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                     return __ldg(p.sB + (col0 / 128) * p.ld_sB + kb);
                 else if constexpr (MODE == DGRAD)
                     return __ldg(p.sB + (int64_t)kb * p.ld_sB + col0 / 128);
-                else if constexpr (MODE == GROUPED)
+                else if constexpr (is_grouped(MODE))
                     return __ldg(p.sB + ((int64_t)tl.expert * (p.N / 128) + col0 / 128) * (p.K / 128) + kb);
                 else
                     return 0.0f;
@@ -589,7 +597,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         // flight; when a block's copies have landed the warp fences them for
         // the tensor cores' async proxy and arrives on the stage's "full"
         // barrier.
-        setmaxnreg_dec<LOW_REGS>();
+        setmaxnreg_dec<Regs<MODE>::LOW>();
         const int wrow = (warp - 2) * 64;          // first tile row of this warp
         const int chunk = lane & 7;                // 16-byte chunk of the row
         int32_t *tok = reinterpret_cast<int32_t *>(smem + SmemLayout::tok_off);
@@ -656,7 +664,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             signal_oldest();
     } else {
         // warps 2..3 complete warpgroup 0 and have no role
-        setmaxnreg_dec<LOW_REGS>();
+        setmaxnreg_dec<Regs<MODE>::LOW>();
     }
 
     tc_fence_before();
@@ -722,7 +730,7 @@ int launch(const CUtensorMap &ta, const CUtensorMap &tb, const Params &p, int gr
         cudaGetLastError();
         return FP8FG_ECUDA;
     }
-    if (fa.numRegs < LAUNCH_REGS_MIN)
+    if (fa.numRegs < Regs<MODE>::LAUNCH_MIN)
         return FP8FG_EUNSUPPORTED;
     k<<<grid, NUM_THREADS, SmemLayout::total, s>>>(ta, tb, p);
     return launch_status();
@@ -876,5 +884,7 @@ extern "C" int fp8_grouped_gemm(const uint8_t *Xq, const float *sX, int64_t ld_s
     if (!make_map(&tb, Wq, (uint64_t)K, (uint64_t)n_experts * (uint64_t)N, (uint64_t)K, BK, BN))
         return FP8FG_ECUDA;
     const int grid = sm_count();
-    return launch_out<GROUPED>(out, ta, tb, p, grid > 0 ? grid : 1, static_cast<cudaStream_t>(stream));
+    if (row_index)
+        return launch_out<GROUPED>(out, ta, tb, p, grid > 0 ? grid : 1, static_cast<cudaStream_t>(stream));
+    return launch_out<GROUPED_C>(out, ta, tb, p, grid > 0 ? grid : 1, static_cast<cudaStream_t>(stream));
 }
