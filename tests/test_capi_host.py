@@ -123,3 +123,57 @@ def test_grouped_validation(L):
     assert call(X=A8) == EALIGN
     assert call(R=0) == 0
     assert call() in (EUNSUPPORTED, 4)
+
+
+def test_quant_dual_validation(L):
+    f = L.fp8_quant_1x128_dual
+    ok = dict(x=A16, rows=256, cols=384, ldx=384, q=A16, ldq=384, s=A16, lds=256, qT=A16, ldqT=256, sT=A16,
+              ldsT=384)
+
+    def call(**kw):
+        a = dict(ok)
+        a.update(kw)
+        return f(a["x"], a["rows"], a["cols"], a["ldx"], a["q"], a["ldq"], a["s"], a["lds"], a["qT"], a["ldqT"],
+                 a["sT"], a["ldsT"], NULL)
+
+    assert call(rows=200, ldqT=200, lds=200) == EINVAL               # rows % 128
+    assert call(cols=200, ldx=200, ldq=200, ldsT=200) == EINVAL      # cols % 128
+    assert call(ldqT=128) == EINVAL                                   # ldqT < rows
+    assert call(ldsT=256) == EINVAL                                   # ld_sT < cols
+    assert call(qT=NULL) == EINVAL
+    assert call(qT=A8) == EALIGN
+    assert call(ldsT=386) == EALIGN
+    assert call(rows=0) == 0
+    assert call() in (EUNSUPPORTED, 4)
+
+
+def test_quant_gather_validation(L):
+    f = L.fp8_quant_1x128_gather
+    ok = dict(x=A16, n_src=16, cols=256, ldx=256, ri=A16, rows=40, q=A16, ldq=256, s=A16, lds=40)
+
+    def call(**kw):
+        a = dict(ok)
+        a.update(kw)
+        return f(a["x"], a["n_src"], a["cols"], a["ldx"], a["ri"], a["rows"], a["q"], a["ldq"], a["s"], a["lds"],
+                 NULL)
+
+    assert call(cols=200, ldx=200, ldq=200) == EINVAL
+    assert call(lds=36) == EINVAL                                     # ld_s < rows
+    assert call(ri=NULL) == EINVAL
+    assert call(n_src=0) == EINVAL                                    # rows to read, no source rows
+    assert call(x=A8) == EALIGN
+    assert call(lds=42) == EALIGN
+    assert call(rows=0) == 0
+    assert call() in (EUNSUPPORTED, 4)
+
+
+def test_grouped_without_row_index_needs_enough_rows(L):
+    # rows already in expert order: row r of Xq feeds output row r, so the
+    # row count may not exceed the rows Xq holds
+    f = L.fp8_grouped_gemm
+
+    def call(T, R):
+        return f(A16, A16, 64, T, NULL, A16, 4, R, A16, A16, 256, 256, A16, 1, 256, NULL)
+
+    assert call(T=60, R=64) == EINVAL
+    assert call(T=64, R=64) in (EUNSUPPORTED, 4)
