@@ -59,6 +59,8 @@ WORKLOADS = {
     "moe": "MoE experts: 4096 tokens, 256 experts 2048x7168, top-8 with Zipf(1.1) bias; quant X + grouped GEMM",
     "outliers": "outlier-heavy fprop: quant 1x128 + block-scaled GEMM, M=16384 K=7168 N=7168, bf16 out",
     "tiny": "tiny fprop: quant X 1x128 + quant W 128x128 + GEMM, 128x256x128, FP32 out",
+    "dense_e4m3": "dense projection fprop, output quantised 1x128 in the GEMM epilogue (E4M3 + scales, the "
+                  "next layer's input): quant X 1x128 + GEMM, M=4096 K=7168 N=7168",
 }
 
 
@@ -169,8 +171,8 @@ def build(workload, dev, seed, fg, synth):
     host copies of e2e (inputs to upload, outputs to download)."""
     import torch
     W = {}
-    if workload in ("dense", "outliers", "tiny"):
-        if workload == "dense":
+    if workload in ("dense", "outliers", "tiny", "dense_e4m3"):
+        if workload in ("dense", "dense_e4m3"):
             x, w = synth.dense(seed=seed, device=dev)
         elif workload == "outliers":
             x, w, _, _ = synth.outliers(seed=seed, device=dev)
@@ -191,9 +193,18 @@ def build(workload, dev, seed, fg, synth):
                               lambda: fg.fp8_quant_128x128(w, q=wq, scales=sw), "hbm", Q128X128_B * Nw * Kx))
         else:
             fg.fp8_quant_128x128(w, q=wq, scales=sw)
-        parts.append(Part("fprop", "gemm_kernel<FPROP>", lambda: fg.fprop(xq, sx, wq, sw, c=y), "tensor",
-                          2.0 * Mx * Nw * Kx))
-        W.update(inputs=[x], outputs=[y], flops=2.0 * Mx * Nw * Kx,
+        if workload == "dense_e4m3":
+            yq = torch.empty((Mx, Nw), dtype=torch.uint8, device=dev)
+            sy = torch.empty((Nw // 128, (Mx + 3) // 4 * 4), dtype=torch.float32, device=dev)
+            parts.append(Part("fprop_e4m3", "gemm_kernel<FPROP, E4M3 out>",
+                              lambda: fg.fp8_gemm_blockscaled_e4m3(fg.FPROP, xq, sx, wq, sw, c=yq, scales=sy),
+                              "tensor", 2.0 * Mx * Nw * Kx))
+            outs = [yq, sy]
+        else:
+            parts.append(Part("fprop", "gemm_kernel<FPROP>", lambda: fg.fprop(xq, sx, wq, sw, c=y), "tensor",
+                              2.0 * Mx * Nw * Kx))
+            outs = [y]
+        W.update(inputs=[x], outputs=outs, flops=2.0 * Mx * Nw * Kx,
                  dims={"M": Mx, "K": Kx, "N": Nw})
     elif workload == "trio":
         x, w, dy = synth.trio(seed=seed, device=dev)
@@ -272,7 +283,7 @@ def build(workload, dev, seed, fg, synth):
 
 def kernel_source_sha():
     h = hashlib.sha256()
-    for f in ("gemm.cu", "quant.cu", "ptx.cuh"):
+    for f in ("gemm.cu", "quant.cu", "ptx.cuh", "group_rule.cuh"):
         with open(os.path.join(ROOT, "fp8_fine_grained_gb300", "csrc", f), "rb") as fh:
             h.update(fh.read())
     return h.hexdigest()[:16]
@@ -356,7 +367,7 @@ def run_ours(args):
     # read-back run at the same time (as a data loader feeding a training
     # or serving loop does); each step still moves all of its bytes.
     e2e = None
-    if args.workload in ("dense", "outliers", "tiny", "trio", "moe"):
+    if args.workload in WORKLOADS:
         sets = [W, build(args.workload, dev, rank, fg, synth)]
         hin = [t.cpu().pin_memory() for t in W["inputs"]]
         hout = [[torch.empty(t.shape, dtype=t.dtype).pin_memory() for t in S["outputs"]] for S in sets]
@@ -486,8 +497,8 @@ def run_ours(args):
 
 def oracle_dims(workload):
     """(M, K, N) of the workload's first GEMM, the one the CPU sample runs."""
-    return {"dense": (4096, 7168, 7168), "outliers": (16384, 7168, 7168), "trio": (8192, 7168, 18432),
-            "moe": (32768, 7168, 2048), "tiny": (128, 256, 128)}[workload]
+    return {"dense": (4096, 7168, 7168), "dense_e4m3": (4096, 7168, 7168), "outliers": (16384, 7168, 7168),
+            "trio": (8192, 7168, 18432), "moe": (32768, 7168, 2048), "tiny": (128, 256, 128)}[workload]
 
 
 def cpu_sample(workload, rows, seed=0):

@@ -46,6 +46,7 @@ def lib():
         L.fp8_quant_1x128_dual.argtypes = [P, I64, I64, I64, P, I64, P, I64, P, I64, P, I64, P]
         L.fp8_quant_128x128.argtypes = [P, I64, I64, I64, P, I64, P, P]
         L.fp8_gemm_blockscaled.argtypes = [I32, P, P, I64, I64, P, P, I64, I64, I64, I64, I64, P, I32, I64, P]
+        L.fp8_gemm_blockscaled_e4m3.argtypes = [I32, P, P, I64, I64, P, P, I64, I64, I64, I64, I64, P, I64, P, I64, P]
         L.fp8_grouped_gemm.argtypes = [P, P, I64, I64, P, P, ctypes.c_int32, I64, P, P, I64, I64, P, I32, I64, P]
         L.fp8fg_status_str.argtypes = [I32]
         L.fp8fg_status_str.restype = ctypes.c_char_p
@@ -230,6 +231,27 @@ def fp8_gemm_blockscaled(mode, a, sa, b, sb, out_dtype=None, c=None, stream=None
                                     c.stride(0), _stream(stream))
     _check(rc, "fp8_gemm_blockscaled")
     return c
+
+
+def fp8_gemm_blockscaled_e4m3(mode, a, sa, b, sb, c=None, scales=None, stream=None):
+    """FPROP or DGRAD with the output quantised in the epilogue: returns
+    (C E4M3 [M,N], scales [N/128, ld_s>=M]), equal to fp8_quant_1x128 of
+    the bf16 output of fp8_gemm_blockscaled."""
+    torch = _torch()
+    for t, n in ((a, "a"), (b, "b"), (sa, "sa"), (sb, "sb")):
+        _rowmajor(t, n)
+    M, K = a.shape
+    N = b.shape[1] if mode == DGRAD else b.shape[0]
+    if c is None:
+        c = torch.empty((M, N), dtype=torch.uint8, device=a.device)
+    if scales is None:
+        scales = torch.empty((N // 128, _pad(max(M, 1), 4)), dtype=torch.float32, device=a.device)
+    _rowmajor(c, "c")
+    rc = lib().fp8_gemm_blockscaled_e4m3(mode, _ptr(a), _ptr(sa), a.stride(0), sa.stride(0), _ptr(b), _ptr(sb),
+                                         b.stride(0), sb.stride(0), M, N, K, _ptr(c), c.stride(0), _ptr(scales),
+                                         scales.stride(0), _stream(stream))
+    _check(rc, "fp8_gemm_blockscaled_e4m3")
+    return c, scales
 
 
 def fprop(xq, sx, wq, sw, out_dtype=None, c=None, stream=None):

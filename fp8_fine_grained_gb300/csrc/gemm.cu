@@ -34,6 +34,7 @@
 // drain their own in-flight copies and MMAs, and release tensor memory.
 #include <cuda_bf16.h>
 
+#include "group_rule.cuh"
 #include "host_common.h"
 #include "ptx.cuh"
 
@@ -75,6 +76,10 @@ constexpr uint32_t STAGE_C_BYTES = 32 * 64;
 // GROUPED_C: MoE experts, A rows already in expert order (TMA tiles). Two
 // instantiations, so that neither carries the other's registers.
 enum Mode { FPROP = 0, DGRAD = 1, WGRAD = 2, GROUPED = 3, GROUPED_C = 4 };
+// Output element: FP32, bf16 (RNE), or E4M3 with 1x128 scales along N (the
+// bf16 value of each element quantised by the group rule, i.e. what
+// fp8_quant_1x128 of the bf16 output would write).
+enum Out { OUT_F32 = 0, OUT_BF16 = 1, OUT_E4M3 = 2 };
 constexpr bool is_grouped(int mode) { return mode == GROUPED || mode == GROUPED_C; }
 
 struct Params {
@@ -96,6 +101,9 @@ struct Params {
     int n_experts;
     int64_t n_rows;
     int64_t n_tokens;
+    // E4M3 output: scales [N/128][ld_sC]
+    float *sC;
+    int64_t ld_sC;
 };
 
 struct SmemLayout {
@@ -228,7 +236,7 @@ __device__ void build_group_prefix(const Params &p, int32_t *prefix)
     __syncthreads();
 }
 
-template <int MODE, bool OUT_BF16>
+template <int MODE, int OUT>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
     gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB, const Params p)
 {
@@ -536,9 +544,25 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             // conflict-free), then the warp reads it back 8 rows x 64 bytes
             // per instruction and stores those runs. Rows past the tile's
             // group (the next expert, or past M) are skipped.
+            float qinv = 1.0f;
+            if constexpr (OUT == OUT_E4M3) {
+                // round to bf16 in place (the values a bf16 store keeps), then
+                // the group rule over this thread's 128 columns: one 1x128
+                // group of its row
+                float amax = 0.0f;
+#pragma unroll
+                for (int a = 0; a < 64; ++a) {
+                    acc[a] = __bfloat1622float2(__float22bfloat162_rn(acc[a]));
+                    amax = fmaxf(amax, fmaxf(fabsf(acc[a].x), fabsf(acc[a].y)));
+                }
+                const ScalePair sp = group_scale(amax);
+                qinv = sp.inv;
+                if (row_ok)
+                    p.sC[(col0 / 128) * p.ld_sC + row] = sp.s;
+            }
             {
-                constexpr int CW = OUT_BF16 ? 32 : 16;   // columns per 64-byte piece of a row
-                constexpr int ESZ = OUT_BF16 ? 2 : 4;
+                constexpr int CW = OUT == OUT_BF16 ? 32 : (OUT == OUT_F32 ? 16 : 64);  // columns per 64-byte piece
+                constexpr int ESZ = OUT == OUT_BF16 ? 2 : (OUT == OUT_F32 ? 4 : 1);
                 uint8_t *const stg = smem + SmemLayout::stage_c_off + ew * STAGE_C_BYTES;
                 // write side: this lane's row, pieces swizzled by (lane / 2) % 4
                 uint8_t *const w_row = stg + lane * 64;
@@ -556,7 +580,17 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 #pragma unroll
                     for (int c = 0; c < 4; ++c) {
                         uint4 o;
-                        if constexpr (OUT_BF16) {
+                        if constexpr (OUT == OUT_E4M3) {
+                            const int a = q * 32 + c * 8;
+                            uint32_t w[4];
+#pragma unroll
+                            for (int k = 0; k < 4; ++k)
+                                w[k] = cvt_e4m3x2(__fmul_rn(acc[a + 2 * k].x, qinv), __fmul_rn(acc[a + 2 * k].y, qinv)) |
+                                       (cvt_e4m3x2(__fmul_rn(acc[a + 2 * k + 1].x, qinv),
+                                                   __fmul_rn(acc[a + 2 * k + 1].y, qinv))
+                                        << 16);
+                            o = make_uint4(w[0], w[1], w[2], w[3]);
+                        } else if constexpr (OUT == OUT_BF16) {
                             const int a = q * 16 + c * 4;
                             __nv_bfloat162 h0 = __float22bfloat162_rn(acc[a + 0]);
                             __nv_bfloat162 h1 = __float22bfloat162_rn(acc[a + 1]);
@@ -714,10 +748,10 @@ bool make_map(CUtensorMap *m, const void *base, uint64_t cols, uint64_t rows, ui
               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-template <int MODE, bool BF16>
+template <int MODE, int OUT>
 int launch(const CUtensorMap &ta, const CUtensorMap &tb, const Params &p, int grid, cudaStream_t s)
 {
-    auto k = gemm_kernel<MODE, BF16>;
+    auto k = gemm_kernel<MODE, OUT>;
     if (cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)SmemLayout::total) !=
         cudaSuccess) {
         cudaGetLastError();
@@ -739,7 +773,7 @@ int launch(const CUtensorMap &ta, const CUtensorMap &tb, const Params &p, int gr
 template <int MODE>
 int launch_out(int out, const CUtensorMap &ta, const CUtensorMap &tb, const Params &p, int grid, cudaStream_t s)
 {
-    return out == FP8FG_OUT_BF16 ? launch<MODE, true>(ta, tb, p, grid, s) : launch<MODE, false>(ta, tb, p, grid, s);
+    return out == FP8FG_OUT_BF16 ? launch<MODE, OUT_BF16>(ta, tb, p, grid, s) : launch<MODE, OUT_F32>(ta, tb, p, grid, s);
 }
 
 bool fill_runtime(Params &p)
@@ -755,18 +789,25 @@ bool fill_runtime(Params &p)
 
 using namespace fp8fg;
 
-extern "C" int fp8_gemm_blockscaled(int mode, const uint8_t *A, const float *sA, int64_t lda, int64_t ld_sA,
-                                    const uint8_t *B, const float *sB, int64_t ldb, int64_t ld_sB, int64_t M,
-                                    int64_t N, int64_t K, void *C, int out, int64_t ldc, void *stream)
+namespace fp8fg {
+namespace {
+
+// shared by the two GEMM entry points; out is an Out kind (sC and ld_sC are
+// read for OUT_E4M3 only)
+int gemm_entry(int mode, const uint8_t *A, const float *sA, int64_t lda, int64_t ld_sA, const uint8_t *B,
+               const float *sB, int64_t ldb, int64_t ld_sB, int64_t M, int64_t N, int64_t K, void *C, int out,
+               int64_t ldc, float *sC, int64_t ld_sC, void *stream)
 {
-    if (mode < FPROP || mode > WGRAD || (out != FP8FG_OUT_F32 && out != FP8FG_OUT_BF16))
+    if (mode < FPROP || mode > WGRAD)
         return FP8FG_EINVAL;
     if (M < 0 || N < 0 || K < BK || N % 128 != 0 || K % BK != 0)
         return FP8FG_EINVAL;
     if (M >= (1ll << 31) || N >= (1ll << 31) || K >= (1ll << 31))
         return FP8FG_EINVAL;
-    const int64_t esz = out == FP8FG_OUT_BF16 ? 2 : 4;
+    const int64_t esz = out == OUT_BF16 ? 2 : (out == OUT_F32 ? 4 : 1);
     if (lda < K || ldc < N || ld_sA < M)
+        return FP8FG_EINVAL;
+    if (out == OUT_E4M3 && ld_sC < M)
         return FP8FG_EINVAL;
     if (mode == DGRAD ? (ldb < N || ld_sB < N / 128) : (ldb < K))
         return FP8FG_EINVAL;
@@ -776,10 +817,12 @@ extern "C" int fp8_gemm_blockscaled(int mode, const uint8_t *A, const float *sA,
         return FP8FG_EINVAL;
     if (M == 0 || N == 0)
         return FP8FG_OK;
-    if (!A || !sA || !B || !sB || !C)
+    if (!A || !sA || !B || !sB || !C || (out == OUT_E4M3 && !sC))
         return FP8FG_EINVAL;
     if (!aligned16(A) || !aligned16(B) || !aligned16(C) || !aligned16(sA) || !aligned16(sB) || lda % 16 != 0 ||
         ldb % 16 != 0 || (ldc * esz) % 16 != 0 || ld_sA % 4 != 0 || (mode == WGRAD && ld_sB % 4 != 0))
+        return FP8FG_EALIGN;
+    if (out == OUT_E4M3 && (!aligned16(sC) || ld_sC % 4 != 0))
         return FP8FG_EALIGN;
     if (!device_supported())
         return FP8FG_EUNSUPPORTED;
@@ -794,6 +837,8 @@ extern "C" int fp8_gemm_blockscaled(int mode, const uint8_t *A, const float *sA,
     p.ld_sB = ld_sB;
     p.C = C;
     p.ldc = ldc;
+    p.sC = sC;
+    p.ld_sC = ld_sC;
     p.num_m_tiles = (M + BM - 1) / BM;
     p.num_n_tiles = (N + BN - 1) / BN;
     if (!fill_runtime(p))
@@ -814,11 +859,36 @@ extern "C" int fp8_gemm_blockscaled(int mode, const uint8_t *A, const float *sA,
     const int sms = sm_count();
     const int grid = (int)(tiles < sms ? tiles : sms);
     cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (out == OUT_E4M3)
+        return mode == FPROP ? launch<FPROP, OUT_E4M3>(ta, tb, p, grid, s) : launch<DGRAD, OUT_E4M3>(ta, tb, p, grid, s);
     switch (mode) {
     case FPROP: return launch_out<FPROP>(out, ta, tb, p, grid, s);
     case DGRAD: return launch_out<DGRAD>(out, ta, tb, p, grid, s);
     default: return launch_out<WGRAD>(out, ta, tb, p, grid, s);
     }
+}
+
+}  // namespace
+}  // namespace fp8fg
+
+extern "C" int fp8_gemm_blockscaled(int mode, const uint8_t *A, const float *sA, int64_t lda, int64_t ld_sA,
+                                    const uint8_t *B, const float *sB, int64_t ldb, int64_t ld_sB, int64_t M,
+                                    int64_t N, int64_t K, void *C, int out, int64_t ldc, void *stream)
+{
+    if (out != FP8FG_OUT_F32 && out != FP8FG_OUT_BF16)
+        return FP8FG_EINVAL;
+    return gemm_entry(mode, A, sA, lda, ld_sA, B, sB, ldb, ld_sB, M, N, K, C, out == FP8FG_OUT_BF16 ? OUT_BF16 : OUT_F32,
+                      ldc, nullptr, 0, stream);
+}
+
+extern "C" int fp8_gemm_blockscaled_e4m3(int mode, const uint8_t *A, const float *sA, int64_t lda, int64_t ld_sA,
+                                         const uint8_t *B, const float *sB, int64_t ldb, int64_t ld_sB, int64_t M,
+                                         int64_t N, int64_t K, uint8_t *Cq, int64_t ldc, float *sC, int64_t ld_sC,
+                                         void *stream)
+{
+    if (mode != FPROP && mode != DGRAD)  // the weight gradient stays FP32
+        return FP8FG_EINVAL;
+    return gemm_entry(mode, A, sA, lda, ld_sA, B, sB, ldb, ld_sB, M, N, K, Cq, OUT_E4M3, ldc, sC, ld_sC, stream);
 }
 
 extern "C" int fp8_grouped_gemm(const uint8_t *Xq, const float *sX, int64_t ld_sX, int64_t n_tokens,

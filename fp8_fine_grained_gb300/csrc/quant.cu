@@ -3,11 +3,8 @@
 // (per column, for the weight-gradient operands), both of those from one
 // read, and 128x128 blocks (weights).
 //
-// Group rule (innerforce.co.kr, fine-grained quantization paragraph, Figure
-// 7(a); tonho.wtf DeepSeek-V3 entry, "como funciona"): amax = max |x| over
-// the group; s = amax/448 and inv = 448/amax as IEEE FP32 divisions (s = inv
-// = 1 when amax is 0 or 448/amax overflows); code = E4M3(x*inv) with one FP32
-// product and one round-to-nearest-even, saturating conversion.
+// The group rule (amax, s = amax/448, inv = 448/amax, one RNE saturating
+// conversion of x*inv) is in group_rule.cuh.
 //
 // The kernels are streams bound by HBM and instruction issue (2 bytes read,
 // 1 byte + 4/128 or 4/16384 bytes written per element). They read with
@@ -16,6 +13,7 @@
 // 32-byte sectors.
 #include <cuda_bf16.h>
 
+#include "group_rule.cuh"
 #include "host_common.h"
 #include "ptx.cuh"
 
@@ -24,23 +22,6 @@ namespace {
 
 constexpr int GROUP = 128;
 
-struct ScalePair {
-    float s, inv;
-};
-
-__device__ __forceinline__ ScalePair group_scale(float amax)
-{
-    ScalePair r{1.0f, 1.0f};
-    if (amax != 0.0f) {
-        float inv = __fdiv_rn(448.0f, amax);
-        if (!isinf(inv)) {
-            r.inv = inv;
-            r.s = __fdiv_rn(amax, 448.0f);
-        }
-    }
-    return r;
-}
-
 // max |x| over 8 bf16 values packed in a uint4 (bit patterns of magnitudes
 // order like the magnitudes themselves).
 __device__ __forceinline__ uint32_t absmax_bits8(const uint4 &v)
@@ -48,11 +29,6 @@ __device__ __forceinline__ uint32_t absmax_bits8(const uint4 &v)
     uint32_t m = __vmaxu2(__vmaxu2(v.x & 0x7FFF7FFFu, v.y & 0x7FFF7FFFu),
                           __vmaxu2(v.z & 0x7FFF7FFFu, v.w & 0x7FFF7FFFu));
     return max(m & 0xFFFFu, m >> 16);
-}
-
-__device__ __forceinline__ uint32_t quant2(uint32_t w, float inv)
-{
-    return cvt_e4m3x2(__fmul_rn(bf16_lo(w), inv), __fmul_rn(bf16_hi(w), inv));
 }
 
 // 8 bf16 -> 8 E4M3 bytes

@@ -210,6 +210,33 @@ FP8FG_API int fp8_gemm_blockscaled(int mode,
                          void *C, int out, int64_t ldc, void *stream);
 
 /* ---------------------------------------------------------------------
+ * fp8_gemm_blockscaled_e4m3: the forward or data-gradient GEMM of
+ * fp8_gemm_blockscaled with its output quantised in the epilogue.
+ * Source: the GEMM above; tonho.wtf "o que isso custou" (the wish to fuse
+ * the FP8 cast with the producer of the activation, so that activations are
+ * stored in FP8 and scaled online); the 1x128 group rule of
+ * fp8_quant_1x128 (innerforce.co.kr, fine-grained quantization paragraph).
+ *
+ * Every element is first rounded to bf16 (RNE), then each row's groups of
+ * 128 consecutive columns are quantised by the 1x128 rule: the outputs are
+ * bit-identical to fp8_quant_1x128 applied to the bf16 result of
+ * fp8_gemm_blockscaled with out = FP8FG_OUT_BF16, without that bf16 matrix
+ * ever being written.
+ *   mode    FP8FG_FPROP or FP8FG_DGRAD (operands as in fp8_gemm_blockscaled;
+ *           FP8FG_WGRAD is EINVAL: the weight gradient stays FP32).
+ *   Cq      E4M3 [M][ldc], ldc >= N, ldc % 16 == 0.
+ *   sC      FP32 [N/128][ld_sC], ld_sC >= M, ld_sC % 4 == 0: scale of row
+ *           r, group g at sC[g*ld_sC + r].
+ *   Other arguments, alignment and errors as fp8_gemm_blockscaled; Cq and sC
+ *   16-byte aligned. Buffers belong to the caller; nothing is allocated.
+ * ------------------------------------------------------------------- */
+FP8FG_API int fp8_gemm_blockscaled_e4m3(int mode,
+                         const uint8_t *A, const float *sA, int64_t lda, int64_t ld_sA,
+                         const uint8_t *B, const float *sB, int64_t ldb, int64_t ld_sB,
+                         int64_t M, int64_t N, int64_t K,
+                         uint8_t *Cq, int64_t ldc, float *sC, int64_t ld_sC, void *stream);
+
+/* ---------------------------------------------------------------------
  * fp8_grouped_gemm: MoE expert GEMM over a per-expert row index.
  * Source: yunhecapital.com 2.2.2 and tonho.wtf "como funciona" (one shared
  * and 256 routed experts, 8 active per token) with the FP8 GEMM above

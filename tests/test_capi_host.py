@@ -177,3 +177,23 @@ def test_grouped_without_row_index_needs_enough_rows(L):
 
     assert call(T=60, R=64) == EINVAL
     assert call(T=64, R=64) in (EUNSUPPORTED, 4)
+
+
+def test_gemm_e4m3_validation(L):
+    f = L.fp8_gemm_blockscaled_e4m3
+
+    def call(**kw):
+        a = dict(mode=0, A=A16, sA=A16, lda=256, ldsa=128, B=A16, sB=A16, ldb=256, ldsb=2, M=128, N=256, K=256,
+                 C=A16, ldc=256, sC=A16, ldsc=128)
+        a.update(kw)
+        return f(a["mode"], a["A"], a["sA"], a["lda"], a["ldsa"], a["B"], a["sB"], a["ldb"], a["ldsb"], a["M"],
+                 a["N"], a["K"], a["C"], a["ldc"], a["sC"], a["ldsc"], NULL)
+
+    assert call(mode=2) == EINVAL                      # wgrad output stays FP32
+    assert call(ldsc=100) == EINVAL                    # ld_sC < M
+    assert call(sC=NULL) == EINVAL
+    assert call(sC=A8) == EALIGN
+    assert call(ldsc=130) == EALIGN
+    assert call(ldc=264) == EALIGN
+    assert call(M=0) == 0
+    assert call() in (EUNSUPPORTED, 4)

@@ -126,6 +126,26 @@ def test_wgrad(tokens, N, K):
     check_gemm(to_np(dw), c, t, False, "wgrad")
 
 
+@pytest.mark.parametrize("mode,M,N,K", [(0, 300, 512, 1024), (0, 129, 384, 512), (1, 200, 384, 640)])
+def test_gemm_e4m3_output(mode, M, N, K):
+    """The GEMM with its output quantised in the epilogue writes exactly
+    what the oracle's 1x128 quantiser makes of the bf16 output of the same
+    GEMM (which itself is checked against the oracle GEMM elsewhere)."""
+    x = _act(M, K, seed=40 + mode)
+    if mode == 0:
+        w = _wt(N, K, seed=41)
+    else:
+        w = _wt(K, N, seed=42)          # dgrad: B is the weight [K_contract][N]
+    xq, sx = fg.fp8_quant_1x128(x)
+    wq, sw = fg.fp8_quant_128x128(w)
+    y = fg.fp8_gemm_blockscaled(mode, xq, sx, wq, sw, out_dtype=torch.bfloat16)
+    yq, sy = fg.fp8_gemm_blockscaled_e4m3(mode, xq, sx, wq, sw)
+    assert fg.device_status() == 0
+    qo, so = oracle.quant_1x128(bits(y))
+    assert np.array_equal(to_np(yq), qo)
+    assert np.array_equal(rows_scales(sy, M).view(np.uint32), so.view(np.uint32))
+
+
 def _moe_small(seed, T=300, K=384, N=256, E=9, counts=None):
     g = _gen(seed)
     x = torch.randn(T, K, generator=g, device=DEV).to(torch.bfloat16)
