@@ -45,9 +45,10 @@ def lib():
         L.orc_e4m3_encode.restype = ctypes.c_uint8
         L.orc_e4m3_encode_array.argtypes = [P, I64, P]
         L.orc_group_scale.argtypes = [ctypes.c_float, P, P]
-        L.orc_quant_1x128.argtypes = [P, I64, I64, P, P]
-        L.orc_quant_128x1_t.argtypes = [P, I64, I64, P, P]
-        L.orc_quant_128x128.argtypes = [P, I64, I64, P, P]
+        L.orc_group_scale_pow2.argtypes = [ctypes.c_float, P, P]
+        L.orc_quant_1x128_rule.argtypes = [P, I64, I64, P, P, ctypes.c_int]
+        L.orc_quant_128x1_t_rule.argtypes = [P, I64, I64, P, P, ctypes.c_int]
+        L.orc_quant_128x128_rule.argtypes = [P, I64, I64, P, P, ctypes.c_int]
         L.orc_gemm_blockscaled.argtypes = [P, P, P, P, I64, I64, I64, P, I64, P, P, P]
         L.orc_f32_to_bf16.argtypes = [P, I64, P]
         L.orc_num_threads.restype = ctypes.c_int
@@ -80,20 +81,26 @@ def e4m3_encode(v):
     return out
 
 
-def group_scale(amax):
-    """(s, inv) for one group with the given amax (float32 scalars)."""
+def group_scale(amax, pow2=False):
+    """(s, inv) for one group with the given amax (float32 scalars).
+
+    pow2=False: the pages' rule, s = amax/448. pow2=True: the microscaling
+    variant, s = the smallest power of two 2^e (e >= -127) with
+    amax <= 448 * s."""
     s = np.zeros(1, np.float32)
     inv = np.zeros(1, np.float32)
-    lib().orc_group_scale(ctypes.c_float(float(np.float32(amax))), _ptr(s), _ptr(inv))
+    fn = lib().orc_group_scale_pow2 if pow2 else lib().orc_group_scale
+    fn(ctypes.c_float(float(np.float32(amax))), _ptr(s), _ptr(inv))
     return s[0], inv[0]
 
 
 # ------------------------------------------------------------ quantise ----
 
-def quant_1x128(x_bits):
+def quant_1x128(x_bits, pow2=False):
     """Per-row 1x128 quantisation.
 
     x_bits: uint16 bf16 bit patterns [rows, cols], cols % 128 == 0.
+    pow2 selects the power-of-two scale rule (see group_scale).
     Returns (q uint8 [rows, cols], s float32 [rows, cols/128]).
     """
     x = _c(x_bits, np.uint16)
@@ -101,12 +108,12 @@ def quant_1x128(x_bits):
     assert cols % GROUP == 0
     q = np.empty((rows, cols), np.uint8)
     s = np.empty((rows, cols // GROUP), np.float32)
-    lib().orc_quant_1x128(_ptr(x), rows, cols, _ptr(q), _ptr(s))
+    lib().orc_quant_1x128_rule(_ptr(x), rows, cols, _ptr(q), _ptr(s), 1 if pow2 else 0)
     return q, s
 
 
-def quant_128x1_t(x_bits):
-    """Groups of 128 rows per column, output transposed.
+def quant_128x1_t(x_bits, pow2=False):
+    """Groups of 128 rows per column, output transposed (pow2: see group_scale).
 
     x_bits: uint16 [rows, cols], rows % 128 == 0.
     Returns (qT uint8 [cols, rows], s float32 [rows/128, cols]).
@@ -116,12 +123,12 @@ def quant_128x1_t(x_bits):
     assert rows % GROUP == 0
     qT = np.empty((cols, rows), np.uint8)
     s = np.empty((rows // GROUP, cols), np.float32)
-    lib().orc_quant_128x1_t(_ptr(x), rows, cols, _ptr(qT), _ptr(s))
+    lib().orc_quant_128x1_t_rule(_ptr(x), rows, cols, _ptr(qT), _ptr(s), 1 if pow2 else 0)
     return qT, s
 
 
-def quant_128x128(w_bits):
-    """128x128 block quantisation.
+def quant_128x128(w_bits, pow2=False):
+    """128x128 block quantisation (pow2: see group_scale).
 
     w_bits: uint16 [N, K], both multiples of 128.
     Returns (q uint8 [N, K], s float32 [N/128, K/128]).
@@ -131,7 +138,7 @@ def quant_128x128(w_bits):
     assert N % GROUP == 0 and K % GROUP == 0
     q = np.empty((N, K), np.uint8)
     s = np.empty((N // GROUP, K // GROUP), np.float32)
-    lib().orc_quant_128x128(_ptr(w), N, K, _ptr(q), _ptr(s))
+    lib().orc_quant_128x128_rule(_ptr(w), N, K, _ptr(q), _ptr(s), 1 if pow2 else 0)
     return q, s
 
 

@@ -37,6 +37,15 @@
  *   - the cross-block FP32 sum runs over blocks in ascending order with a
  *     separate multiply and add (no fused multiply-add).
  *
+ * Microscaling variant ([innerforce], the paragraph that relates the
+ * fine-grained groups to microscaling formats and to the Blackwell tensor
+ * cores that support them; [tonho] "o que isso custou": tensor-core MMA with
+ * group scaling is on the wish list, "onde isso aparece hoje": microscaling
+ * announced for Blackwell). Microscaling shares one power-of-two scale per
+ * group. Reading: the same 1x128 / 128x128 groups, each scale the smallest
+ * power of two 2^e (e >= -127) with amax <= 448 * 2^e; amax = 0 gives s = 1.
+ * x * 2^-e is exact, so a code is one rounding of x/s into E4M3.
+ *
  * Build: gcc -O2 -std=c11 -ffp-contract=off -fopenmp -shared -fPIC.
  * -ffp-contract=off matters: the FP32 accumulation below is specified as a
  * rounded product followed by a rounded sum.
@@ -140,6 +149,36 @@ void orc_group_scale(float amax, float *s, float *inv)
     *inv = i;
 }
 
+/* Power-of-two scale of one group (the microscaling variant): the smallest
+ * s = 2^e, e >= -127, with amax <= 448 * s; inv = 1/s. Both are exact.
+ * frexpf gives amax = f * 2^x with f in [0.5, 1), so amax * 2^-(x-9) lies in
+ * [256, 512): e is x-9, or x-8 when that product exceeds 448. */
+void orc_group_scale_pow2(float amax, float *s, float *inv)
+{
+    int x, e;
+    if (amax == 0.0f) {
+        *s = 1.0f;
+        *inv = 1.0f;
+        return;
+    }
+    (void)frexpf(amax, &x);
+    e = x - 9;
+    if (ldexpf(amax, -e) > 448.0f)
+        e += 1;
+    if (e < -127)
+        e = -127;
+    *s = ldexpf(1.0f, e);
+    *inv = ldexpf(1.0f, -e);
+}
+
+typedef void (*scale_rule_fn)(float, float *, float *);
+
+/* rule 0: s = amax/448 (the pages' method); rule 1: power of two */
+static scale_rule_fn scale_rule(int rule)
+{
+    return rule ? orc_group_scale_pow2 : orc_group_scale;
+}
+
 /* One element: a single FP32 product by inv, then one rounding into E4M3. */
 static uint8_t quantise_one(float x, float inv)
 {
@@ -150,10 +189,11 @@ static uint8_t quantise_one(float x, float inv)
 /* 1x128 tiles: per row, per group of 128 consecutive columns.
  * x: bf16 bits [rows][cols]; q: codes [rows][cols]; s: scales [rows][cols/128].
  * cols must be a multiple of 128. */
-void orc_quant_1x128(const uint16_t *x, int64_t rows, int64_t cols,
-                     uint8_t *q, float *s)
+void orc_quant_1x128_rule(const uint16_t *x, int64_t rows, int64_t cols,
+                          uint8_t *q, float *s, int rule)
 {
     int64_t groups = cols / ORC_GROUP;
+    scale_rule_fn group_scale = scale_rule(rule);
 #pragma omp parallel for schedule(static)
     for (int64_t r = 0; r < rows; ++r) {
         for (int64_t g = 0; g < groups; ++g) {
@@ -164,7 +204,7 @@ void orc_quant_1x128(const uint16_t *x, int64_t rows, int64_t cols,
                 if (a > amax)
                     amax = a;
             }
-            orc_group_scale(amax, &sc, &inv);
+            group_scale(amax, &sc, &inv);
             s[r * groups + g] = sc;
             for (int k = 0; k < ORC_GROUP; ++k)
                 q[r * cols + g * ORC_GROUP + k] = quantise_one(bf16_to_f32(xg[k]), inv);
@@ -176,10 +216,11 @@ void orc_quant_1x128(const uint16_t *x, int64_t rows, int64_t cols,
  * operands of the weight-gradient GEMM, which contracts over tokens.
  * x: bf16 bits [rows][cols]; qT: codes [cols][rows]; s: scales
  * [rows/128][cols]. rows must be a multiple of 128. */
-void orc_quant_128x1_t(const uint16_t *x, int64_t rows, int64_t cols,
-                       uint8_t *qT, float *s)
+void orc_quant_128x1_t_rule(const uint16_t *x, int64_t rows, int64_t cols,
+                            uint8_t *qT, float *s, int rule)
 {
     int64_t groups = rows / ORC_GROUP;
+    scale_rule_fn group_scale = scale_rule(rule);
 #pragma omp parallel for schedule(static)
     for (int64_t c = 0; c < cols; ++c) {
         for (int64_t g = 0; g < groups; ++g) {
@@ -189,7 +230,7 @@ void orc_quant_128x1_t(const uint16_t *x, int64_t rows, int64_t cols,
                 if (a > amax)
                     amax = a;
             }
-            orc_group_scale(amax, &sc, &inv);
+            group_scale(amax, &sc, &inv);
             s[g * cols + c] = sc;
             for (int k = 0; k < ORC_GROUP; ++k) {
                 int64_t r = g * ORC_GROUP + k;
@@ -202,10 +243,11 @@ void orc_quant_128x1_t(const uint16_t *x, int64_t rows, int64_t cols,
 /* 128x128 blocks ([innerforce]: per 128 input channels per 128 output
  * channels). w: bf16 bits [N][K]; q: codes [N][K]; s: scales [N/128][K/128].
  * N and K must be multiples of 128. */
-void orc_quant_128x128(const uint16_t *w, int64_t N, int64_t K,
-                       uint8_t *q, float *s)
+void orc_quant_128x128_rule(const uint16_t *w, int64_t N, int64_t K,
+                            uint8_t *q, float *s, int rule)
 {
     int64_t nb = N / ORC_GROUP, kb = K / ORC_GROUP;
+    scale_rule_fn group_scale = scale_rule(rule);
 #pragma omp parallel for collapse(2) schedule(static)
     for (int64_t bi = 0; bi < nb; ++bi) {
         for (int64_t bj = 0; bj < kb; ++bj) {
@@ -216,7 +258,7 @@ void orc_quant_128x128(const uint16_t *w, int64_t N, int64_t K,
                     if (a > amax)
                         amax = a;
                 }
-            orc_group_scale(amax, &sc, &inv);
+            group_scale(amax, &sc, &inv);
             s[bi * kb + bj] = sc;
             for (int i = 0; i < ORC_GROUP; ++i)
                 for (int j = 0; j < ORC_GROUP; ++j) {
@@ -225,6 +267,22 @@ void orc_quant_128x128(const uint16_t *w, int64_t N, int64_t K,
                 }
         }
     }
+}
+
+/* The pages' scale rule (rule 0) under the original names. */
+void orc_quant_1x128(const uint16_t *x, int64_t rows, int64_t cols, uint8_t *q, float *s)
+{
+    orc_quant_1x128_rule(x, rows, cols, q, s, 0);
+}
+
+void orc_quant_128x1_t(const uint16_t *x, int64_t rows, int64_t cols, uint8_t *qT, float *s)
+{
+    orc_quant_128x1_t_rule(x, rows, cols, qT, s, 0);
+}
+
+void orc_quant_128x128(const uint16_t *w, int64_t N, int64_t K, uint8_t *q, float *s)
+{
+    orc_quant_128x128_rule(w, N, K, q, s, 0);
 }
 
 /* ---------------------------------------------------------------------- */

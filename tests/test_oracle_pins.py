@@ -270,6 +270,98 @@ def test_128x128_block_membership_and_transpose():
     assert s3[1, 2] == np.float32(64.0 / 448.0)
 
 
+# ------------------------------------------- power-of-two scale variant ----
+# The microscaling variant keeps the pages' groups but shares one power-of-two
+# scale per group: s = 2^e, the smallest with amax <= 448 * 2^e (e >= -127).
+
+def test_pow2_scale_hand_derived_values():
+    # (amax, e) worked out by hand from "smallest e with amax <= 448 * 2^e"
+    cases = [
+        (448.0, 0),                      # exactly 448 * 2^0
+        (450.0, 1),                      # next bf16 above 448
+        (224.0, -1),                     # 448 * 2^-1 = 224 covers it, 112 does not
+        (1.0, -8),                       # 448/256 = 1.75 >= 1 > 448/512
+        (1.75, -8),                      # 448 * 2^-8 = 1.75 exactly
+        (1.7578125, -7),                 # the bf16 just above 1.75
+        (0.01, -15),                     # 448 * 2^-16 = 0.00684 < 0.01 <= 0.01367
+        (3.3895313892515355e38, 120),    # largest finite bf16, 1.9921875 * 2^127
+        (1.75 * 2.0 ** -119, -127),      # 448 * 2^-127 exactly
+        (2.0 ** -120, -127),             # below 448 * 2^-128: clamped to -127
+        (2.0 ** -133, -127),             # smallest bf16 subnormal
+    ]
+    for amax, e in cases:
+        s, inv = oracle.group_scale(np.float32(amax), pow2=True)
+        assert Fraction(float(s)) == Fraction(2) ** e, (amax, e, s)
+        assert Fraction(float(inv)) == Fraction(2) ** -e, (amax, e, inv)
+    assert oracle.group_scale(0.0, pow2=True) == (1.0, 1.0)
+
+
+def test_pow2_scale_is_the_smallest_power_covering_amax():
+    rng = np.random.default_rng(11)
+    bits = rng.integers(1, 0x7F80, size=4000, dtype=np.int64).astype(np.uint16)  # finite positive bf16
+    for a in bits_to_f32(bits):
+        s, inv = oracle.group_scale(a, pow2=True)
+        fa, fs = Fraction(float(a)), Fraction(float(s))
+        m, x = np.frexp(float(s))
+        assert m == 0.5 and Fraction(float(inv)) * fs == 1
+        assert fa <= 448 * fs
+        e = x - 1
+        assert e == -127 or fa > 448 * fs / 2
+
+
+def test_pow2_codes_are_one_rounding_of_x_over_s():
+    """code = RNE(x / s) with s = 2^e; x/s <= 448 so nothing saturates."""
+    rng = np.random.default_rng(12)
+    x = (rng.standard_normal((6, 512)) * np.exp(3 * rng.standard_normal(512))).astype(np.float32)
+    x[0, :128] = 0.0
+    x[1, 128:256] *= np.float32(1e-30)
+    b = bf16_bits_of(x)
+    q, s = oracle.quant_1x128(b, pow2=True)
+    xf = bits_to_f32(b).astype(np.float64)
+    sr = np.repeat(s, 128, axis=1).astype(np.float64)
+    y = xf / sr                                   # exact: division by a power of two
+    assert np.all(np.abs(y) <= 448.0)
+    assert np.array_equal(q, torch_e4m3(y.astype(np.float32)))
+    assert s[0, 0] == 1.0 and np.all(q[0, :128] == 0)
+
+
+def test_pow2_fp8_representable_groups_roundtrip():
+    dec = oracle.e4m3_decode_table()
+    rng = np.random.default_rng(13)
+    codes = finite_codes()
+    for e in (-20, -8, 0, 5):
+        src = rng.choice(codes, size=(3, 256))
+        src[:, 3] = 0x7E
+        src[:, 200] = 0xFE
+        x = dec[src] * np.float32(2.0 ** e)
+        q, s = oracle.quant_1x128(bf16_bits_of(x), pow2=True)
+        assert np.array_equal(dec[q], dec[src])
+        assert np.all(s == np.float32(2.0 ** e))
+    # an amax one bf16 step above 448 * 2^e moves the scale to 2^(e+1)
+    x = dec[rng.choice(codes, size=(1, 128))].astype(np.float32)
+    x[0, 7] = 450.0
+    _, s = oracle.quant_1x128(bf16_bits_of(x), pow2=True)
+    assert s[0, 0] == 2.0
+
+
+def test_pow2_layouts_agree_with_rowwise():
+    rng = np.random.default_rng(14)
+    x = (rng.standard_normal((256, 384)) * np.exp(rng.standard_normal(384))).astype(np.float32)
+    b = bf16_bits_of(x)
+    qT, sT = oracle.quant_128x1_t(b, pow2=True)
+    q_ref, s_ref = oracle.quant_1x128(np.ascontiguousarray(b.T), pow2=True)
+    assert np.array_equal(qT, q_ref) and np.array_equal(sT, s_ref.T)
+    qb, sb = oracle.quant_128x128(b, pow2=True)
+    xf = bits_to_f32(b)
+    for bi in range(2):
+        for bj in range(3):
+            blk = xf[bi * 128:(bi + 1) * 128, bj * 128:(bj + 1) * 128]
+            s, inv = oracle.group_scale(np.abs(blk).max(), pow2=True)
+            assert sb[bi, bj] == s
+            assert np.array_equal(qb[bi * 128:(bi + 1) * 128, bj * 128:(bj + 1) * 128],
+                                  torch_e4m3(blk.astype(np.float64) / float(s)))
+
+
 # ------------------------------------------------------------------- GEMM ----
 
 def _rand_codes(rng, shape):
