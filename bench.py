@@ -20,6 +20,11 @@ Other workloads, one JSON line each, for the remaining kernels:
               (1x128, one pass) + grouped expert GEMM
     outliers  M = 16384 fprop with outlier channels and weight blocks
     tiny      128 x 256 x 128 fprop, FP32 out (latency)
+    dense_e4m3  the dense step with the GEMM's output quantised 1x128 in its
+              epilogue
+    dense_mx, trio_mx  the dense and trio steps in the microscaling variant:
+              power-of-two group scales, GEMMs on the tensor cores'
+              block-scaled MMA (no per-block promotion)
 
 Every kernel of a step is timed with CUDA events on the launching stream; L2
 is flushed between steps (a 512 MiB write, then a 256 MiB read so that no
@@ -27,7 +32,7 @@ dirty lines are written back inside the next step), outside the events.
 
 Usage:
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
-                    [--workload dense|trio|moe|outliers|tiny]
+                    [--workload dense|trio|moe|outliers|tiny|dense_e4m3|dense_mx|trio_mx]
 Under torchrun (N > 1) every rank runs its own replica of the workload
 (weak scaling, no data-path collective); times are the max over ranks.
 ``--impl reference`` times the CPU oracle on a bounded sample of the same
@@ -61,6 +66,10 @@ WORKLOADS = {
     "tiny": "tiny fprop: quant X 1x128 + quant W 128x128 + GEMM, 128x256x128, FP32 out",
     "dense_e4m3": "dense projection fprop, output quantised 1x128 in the GEMM epilogue (E4M3 + scales, the "
                   "next layer's input): quant X 1x128 + GEMM, M=4096 K=7168 N=7168",
+    "dense_mx": "dense projection fprop, microscaling variant (power-of-two scales, tensor-core block "
+                "scaling): quant 1x128 + GEMM, M=4096 K=7168 N=7168, bf16 out",
+    "trio_mx": "linear 7168->18432 at M=8192, microscaling variant (power-of-two scales, tensor-core block "
+               "scaling): quant W 128x128, X/dY 1x128 and transposed; fprop, dgrad, wgrad",
 }
 
 
@@ -171,6 +180,9 @@ def build(workload, dev, seed, fg, synth):
     host copies of e2e (inputs to upload, outputs to download)."""
     import torch
     W = {}
+    mx = workload.endswith("_mx")           # power-of-two scales, block-scaled MMA
+    if mx:
+        workload = workload[:-3]
     if workload in ("dense", "outliers", "tiny", "dense_e4m3"):
         if workload in ("dense", "dense_e4m3"):
             x, w = synth.dense(seed=seed, device=dev)
@@ -186,13 +198,13 @@ def build(workload, dev, seed, fg, synth):
         wq = torch.empty((Nw, Kx), dtype=torch.uint8, device=dev)
         sw = torch.empty((Nw // 128, Kx // 128), dtype=torch.float32, device=dev)
         y = torch.empty((Mx, Nw), dtype=out_dt, device=dev)
-        parts = [Part("quant_x_1x128", "quant_rows_kernel", lambda: fg.fp8_quant_1x128(x, q=xq, scales=sx),
-                      "hbm", Q1X128_B * Mx * Kx)]
+        parts = [Part("quant_x_1x128", "quant_rows_kernel",
+                      lambda: fg.fp8_quant_1x128(x, q=xq, scales=sx, pow2=mx), "hbm", Q1X128_B * Mx * Kx)]
         if workload == "tiny":
             parts.append(Part("quant_w_128x128", "quant_blocks_kernel",
                               lambda: fg.fp8_quant_128x128(w, q=wq, scales=sw), "hbm", Q128X128_B * Nw * Kx))
         else:
-            fg.fp8_quant_128x128(w, q=wq, scales=sw)
+            fg.fp8_quant_128x128(w, q=wq, scales=sw, pow2=mx)
         if workload == "dense_e4m3":
             yq = torch.empty((Mx, Nw), dtype=torch.uint8, device=dev)
             sy = torch.empty((Nw // 128, (Mx + 3) // 4 * 4), dtype=torch.float32, device=dev)
@@ -200,6 +212,10 @@ def build(workload, dev, seed, fg, synth):
                               lambda: fg.fp8_gemm_blockscaled_e4m3(fg.FPROP, xq, sx, wq, sw, c=yq, scales=sy),
                               "tensor", 2.0 * Mx * Nw * Kx))
             outs = [yq, sy]
+        elif mx:
+            parts.append(Part("fprop", "gemm_mx_kernel<FPROP>",
+                              lambda: fg.fp8_gemm_mx(fg.FPROP, xq, sx, wq, sw, c=y), "tensor", 2.0 * Mx * Nw * Kx))
+            outs = [y]
         else:
             parts.append(Part("fprop", "gemm_kernel<FPROP>", lambda: fg.fprop(xq, sx, wq, sw, c=y), "tensor",
                               2.0 * Mx * Nw * Kx))
@@ -224,20 +240,23 @@ def build(workload, dev, seed, fg, synth):
         dx = torch.empty((Mx, Kx), dtype=torch.bfloat16, device=dev)
         dw = torch.empty((Nw, Kx), dtype=torch.float32, device=dev)
         f = 2.0 * Mx * Nw * Kx
+        gemm = (lambda mode, *a, c: fg.fp8_gemm_mx(mode, *a, c=c)) if mx else \
+            (lambda mode, *a, c: fg.fp8_gemm_blockscaled(mode, *a, c=c))
+        gk = "gemm_mx_kernel" if mx else "gemm_kernel"
         parts = [
-            Part("quant_w_128x128", "quant_blocks_kernel", lambda: fg.fp8_quant_128x128(w, q=wq, scales=sw),
-                 "hbm", Q128X128_B * Nw * Kx),
+            Part("quant_w_128x128", "quant_blocks_kernel",
+                 lambda: fg.fp8_quant_128x128(w, q=wq, scales=sw, pow2=mx), "hbm", Q128X128_B * Nw * Kx),
             # X and dY each read once for both layouts (1x128 rows for
             # fprop/dgrad, 128x1 transposed for wgrad)
             Part("quant_x_dual", "quant_dual_kernel",
-                 lambda: fg.fp8_quant_1x128_dual(x, q=xq, scales=sx, qT=xqT, scalesT=sxT), "hbm",
+                 lambda: fg.fp8_quant_1x128_dual(x, q=xq, scales=sx, qT=xqT, scalesT=sxT, pow2=mx), "hbm",
                  QDUAL_B * Mx * Kx),
             Part("quant_dy_dual", "quant_dual_kernel",
-                 lambda: fg.fp8_quant_1x128_dual(dy, q=dyq, scales=sdy, qT=dyqT, scalesT=sdyT), "hbm",
+                 lambda: fg.fp8_quant_1x128_dual(dy, q=dyq, scales=sdy, qT=dyqT, scalesT=sdyT, pow2=mx), "hbm",
                  QDUAL_B * Mx * Nw),
-            Part("fprop", "gemm_kernel<FPROP>", lambda: fg.fprop(xq, sx, wq, sw, c=y), "tensor", f),
-            Part("dgrad", "gemm_kernel<DGRAD>", lambda: fg.dgrad(dyq, sdy, wq, sw, c=dx), "tensor", f),
-            Part("wgrad", "gemm_kernel<WGRAD>", lambda: fg.wgrad(dyqT, sdyT, xqT, sxT, c=dw), "tensor", f),
+            Part("fprop", gk + "<FPROP>", lambda: gemm(fg.FPROP, xq, sx, wq, sw, c=y), "tensor", f),
+            Part("dgrad", gk + "<DGRAD>", lambda: gemm(fg.DGRAD, dyq, sdy, wq, sw, c=dx), "tensor", f),
+            Part("wgrad", gk + "<WGRAD>", lambda: gemm(fg.WGRAD, dyqT, sdyT, xqT, sxT, c=dw), "tensor", f),
         ]
         W.update(inputs=[x, dy], outputs=[y, dx, dw], flops=3 * f, dims={"M": Mx, "K": Kx, "N": Nw})
     elif workload == "moe":
@@ -283,7 +302,7 @@ def build(workload, dev, seed, fg, synth):
 
 def kernel_source_sha():
     h = hashlib.sha256()
-    for f in ("gemm.cu", "quant.cu", "ptx.cuh", "group_rule.cuh"):
+    for f in ("gemm.cu", "gemm_mx.cu", "quant.cu", "ptx.cuh", "group_rule.cuh"):
         with open(os.path.join(ROOT, "fp8_fine_grained_gb300", "csrc", f), "rb") as fh:
             h.update(fh.read())
     return h.hexdigest()[:16]
@@ -498,7 +517,8 @@ def run_ours(args):
 def oracle_dims(workload):
     """(M, K, N) of the workload's first GEMM, the one the CPU sample runs."""
     return {"dense": (4096, 7168, 7168), "dense_e4m3": (4096, 7168, 7168), "outliers": (16384, 7168, 7168),
-            "trio": (8192, 7168, 18432), "moe": (32768, 7168, 2048), "tiny": (128, 256, 128)}[workload]
+            "trio": (8192, 7168, 18432), "moe": (32768, 7168, 2048), "tiny": (128, 256, 128),
+            "dense_mx": (4096, 7168, 7168), "trio_mx": (8192, 7168, 18432)}[workload]
 
 
 def cpu_sample(workload, rows, seed=0):
@@ -511,16 +531,17 @@ def cpu_sample(workload, rows, seed=0):
     from fp8_fine_grained_gb300 import synth
 
     M, K, N = oracle_dims(workload)
+    pow2 = workload.endswith("_mx")
     rows = min(rows, M)
     g = torch.Generator()
     g.manual_seed(seed)
     c = torch.exp(torch.randn(K, generator=g))
     xs = (torch.randn(rows, K, generator=g) * c).to(torch.bfloat16)
     w = (torch.randn(N, K, generator=g) * 0.02).to(torch.bfloat16)
-    wq, sw = oracle.quant_128x128(synth.bf16_bits(w))
+    wq, sw = oracle.quant_128x128(synth.bf16_bits(w), pow2=pow2)
     xb = synth.bf16_bits(xs)
     t0 = time.perf_counter()
-    xq, sx = oracle.quant_1x128(xb)
+    xq, sx = oracle.quant_1x128(xb, pow2=pow2)
     oracle.fprop(xq, sx, wq, sw, want_exact=False)
     dt = time.perf_counter() - t0
     return dt, 2.0 * rows * N * K, oracle.num_threads()

@@ -45,6 +45,11 @@ def lib():
         L.fp8_quant_1x128_gather.argtypes = [P, I64, I64, I64, P, I64, P, I64, P, I64, P]
         L.fp8_quant_1x128_dual.argtypes = [P, I64, I64, I64, P, I64, P, I64, P, I64, P, I64, P]
         L.fp8_quant_128x128.argtypes = [P, I64, I64, I64, P, I64, P, P]
+        L.fp8_quant_1x128_pow2.argtypes = L.fp8_quant_1x128.argtypes
+        L.fp8_quant_1x128_gather_pow2.argtypes = L.fp8_quant_1x128_gather.argtypes
+        L.fp8_quant_1x128_dual_pow2.argtypes = L.fp8_quant_1x128_dual.argtypes
+        L.fp8_quant_128x128_pow2.argtypes = L.fp8_quant_128x128.argtypes
+        L.fp8_gemm_mx.argtypes = [I32, P, P, I64, I64, P, P, I64, I64, I64, I64, I64, P, I32, I64, P]
         L.fp8_gemm_blockscaled.argtypes = [I32, P, P, I64, I64, P, P, I64, I64, I64, I64, I64, P, I32, I64, P]
         L.fp8_gemm_blockscaled_e4m3.argtypes = [I32, P, P, I64, I64, P, P, I64, I64, I64, I64, I64, P, I64, P, I64, P]
         L.fp8_grouped_gemm.argtypes = [P, P, I64, I64, P, P, ctypes.c_int32, I64, P, P, I64, I64, P, I32, I64, P]
@@ -99,8 +104,10 @@ def _pad(n, m):
 
 # ------------------------------------------------------------- quantise ----
 
-def fp8_quant_1x128(x, transpose=False, q=None, scales=None, stream=None):
+def fp8_quant_1x128(x, transpose=False, q=None, scales=None, stream=None, pow2=False):
     """E4M3 codes and FP32 scales of a bf16 matrix in 1x128 tiles.
+
+    pow2=True selects the power-of-two scale rule (fp8_quant_1x128_pow2).
 
     transpose=False: x [rows, cols] grouped per row along cols (cols % 128 == 0);
         returns q uint8 [rows, cols], scales float32 [cols/128, ld_s>=rows].
@@ -122,16 +129,18 @@ def fp8_quant_1x128(x, transpose=False, q=None, scales=None, stream=None):
             q = torch.empty((cols, rows), dtype=torch.uint8, device=x.device)
         if scales is None:
             scales = torch.empty((rows // 128, _pad(max(cols, 1), 4)), dtype=torch.float32, device=x.device)
-    rc = lib().fp8_quant_1x128(_ptr(x), rows, cols, x.stride(0), _ptr(q), q.stride(0), _ptr(scales),
-                               scales.stride(0), 1 if transpose else 0, _stream(stream))
-    _check(rc, "fp8_quant_1x128")
+    fn = lib().fp8_quant_1x128_pow2 if pow2 else lib().fp8_quant_1x128
+    rc = fn(_ptr(x), rows, cols, x.stride(0), _ptr(q), q.stride(0), _ptr(scales),
+            scales.stride(0), 1 if transpose else 0, _stream(stream))
+    _check(rc, "fp8_quant_1x128_pow2" if pow2 else "fp8_quant_1x128")
     return q, scales
 
 
-def fp8_quant_1x128_dual(x, q=None, scales=None, qT=None, scalesT=None, stream=None):
+def fp8_quant_1x128_dual(x, q=None, scales=None, qT=None, scalesT=None, stream=None, pow2=False):
     """Both layouts of fp8_quant_1x128 from one read of x (rows and cols
     multiples of 128): returns (q, scales, qT, scalesT), equal to
-    fp8_quant_1x128(x) and fp8_quant_1x128(x, transpose=True)."""
+    fp8_quant_1x128(x) and fp8_quant_1x128(x, transpose=True) (with the
+    same pow2 choice)."""
     torch = _torch()
     _rowmajor(x, "x")
     if x.dtype != torch.bfloat16:
@@ -146,14 +155,15 @@ def fp8_quant_1x128_dual(x, q=None, scales=None, qT=None, scalesT=None, stream=N
         qT = torch.empty((cols, rows), dtype=torch.uint8, device=dev)
     if scalesT is None:
         scalesT = torch.empty((rows // 128, _pad(max(cols, 1), 4)), dtype=torch.float32, device=dev)
-    rc = lib().fp8_quant_1x128_dual(_ptr(x), rows, cols, x.stride(0), _ptr(q), q.stride(0), _ptr(scales),
-                                    scales.stride(0), _ptr(qT), qT.stride(0), _ptr(scalesT), scalesT.stride(0),
-                                    _stream(stream))
-    _check(rc, "fp8_quant_1x128_dual")
+    fn = lib().fp8_quant_1x128_dual_pow2 if pow2 else lib().fp8_quant_1x128_dual
+    rc = fn(_ptr(x), rows, cols, x.stride(0), _ptr(q), q.stride(0), _ptr(scales),
+            scales.stride(0), _ptr(qT), qT.stride(0), _ptr(scalesT), scalesT.stride(0),
+            _stream(stream))
+    _check(rc, "fp8_quant_1x128_dual_pow2" if pow2 else "fp8_quant_1x128_dual")
     return q, scales, qT, scalesT
 
 
-def fp8_quant_1x128_gather(x, row_index, q=None, scales=None, stream=None):
+def fp8_quant_1x128_gather(x, row_index, q=None, scales=None, stream=None, pow2=False):
     """1x128 quantisation of the rows x[row_index[r]], written in row_index
     order (MoE rows grouped by expert): q uint8 [n_rows, cols], scales
     float32 [cols/128, ld_s>=n_rows]. Equal to gathering the rows of
@@ -170,13 +180,14 @@ def fp8_quant_1x128_gather(x, row_index, q=None, scales=None, stream=None):
         q = torch.empty((rows, cols), dtype=torch.uint8, device=x.device)
     if scales is None:
         scales = torch.empty((cols // 128, _pad(max(rows, 1), 4)), dtype=torch.float32, device=x.device)
-    rc = lib().fp8_quant_1x128_gather(_ptr(x), n_src, cols, x.stride(0), _ptr(row_index), rows, _ptr(q),
-                                      q.stride(0), _ptr(scales), scales.stride(0), _stream(stream))
-    _check(rc, "fp8_quant_1x128_gather")
+    fn = lib().fp8_quant_1x128_gather_pow2 if pow2 else lib().fp8_quant_1x128_gather
+    rc = fn(_ptr(x), n_src, cols, x.stride(0), _ptr(row_index), rows, _ptr(q),
+            q.stride(0), _ptr(scales), scales.stride(0), _stream(stream))
+    _check(rc, "fp8_quant_1x128_gather_pow2" if pow2 else "fp8_quant_1x128_gather")
     return q, scales
 
 
-def fp8_quant_128x128(w, q=None, scales=None, stream=None):
+def fp8_quant_128x128(w, q=None, scales=None, stream=None, pow2=False):
     """E4M3 codes and FP32 scales of a bf16 weight [N, K] in 128x128 blocks.
     A 3-D weight [E, N, K] (MoE experts) is quantised as [E*N, K]."""
     torch = _torch()
@@ -192,9 +203,9 @@ def fp8_quant_128x128(w, q=None, scales=None, stream=None):
         scales = torch.empty(tuple(shape[:-2]) + (shape[-2] // 128, K // 128), dtype=torch.float32,
                              device=w.device)
     q2 = q.reshape(-1, K)
-    rc = lib().fp8_quant_128x128(_ptr(w2), N, K, w2.stride(0), _ptr(q2), q2.stride(0), _ptr(scales),
-                                 _stream(stream))
-    _check(rc, "fp8_quant_128x128")
+    fn = lib().fp8_quant_128x128_pow2 if pow2 else lib().fp8_quant_128x128
+    rc = fn(_ptr(w2), N, K, w2.stride(0), _ptr(q2), q2.stride(0), _ptr(scales), _stream(stream))
+    _check(rc, "fp8_quant_128x128_pow2" if pow2 else "fp8_quant_128x128")
     return q, scales
 
 
@@ -230,6 +241,27 @@ def fp8_gemm_blockscaled(mode, a, sa, b, sb, out_dtype=None, c=None, stream=None
                                     b.stride(0), sb.stride(0), M, N, K, _ptr(c), _out_code(c.dtype),
                                     c.stride(0), _stream(stream))
     _check(rc, "fp8_gemm_blockscaled")
+    return c
+
+
+def fp8_gemm_mx(mode, a, sa, b, sb, out_dtype=None, c=None, stream=None):
+    """fp8_gemm_blockscaled's GEMM for power-of-two scales (the *_pow2
+    quantisers' output), with the scales applied by the tensor cores'
+    block-scaled MMA; same modes, shapes and layouts."""
+    torch = _torch()
+    for t, n in ((a, "a"), (b, "b"), (sa, "sa"), (sb, "sb")):
+        _rowmajor(t, n)
+    M, K = a.shape
+    N = b.shape[1] if mode == DGRAD else b.shape[0]
+    if out_dtype is None:
+        out_dtype = torch.float32 if mode == WGRAD else torch.bfloat16
+    if c is None:
+        c = torch.empty((M, N), dtype=out_dtype, device=a.device)
+    _rowmajor(c, "c")
+    rc = lib().fp8_gemm_mx(mode, _ptr(a), _ptr(sa), a.stride(0), sa.stride(0), _ptr(b), _ptr(sb),
+                           b.stride(0), sb.stride(0), M, N, K, _ptr(c), _out_code(c.dtype),
+                           c.stride(0), _stream(stream))
+    _check(rc, "fp8_gemm_mx")
     return c
 
 

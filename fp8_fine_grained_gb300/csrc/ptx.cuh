@@ -322,6 +322,57 @@ __host__ __device__ constexpr uint32_t idesc_e4m3_f32(int M, int N, bool b_mn_ma
            | ((uint32_t)(M >> 4) << 24);              // M / 16
 }
 
+// Instruction descriptor for kind::mxf8f6f4 with block scaling: E4M3 x E4M3
+// -> FP32, M x N tile, UE8M0 scale factors; the scale-factor byte selectors
+// of A (bits 29-30) and B (bits 4-5) are 0.
+__host__ __device__ constexpr uint32_t idesc_mx_e4m3(int M, int N, bool b_mn_major)
+{
+    return (0u << 4)                                  // B scale-factor byte 0
+           | (0u << 7)                                // A: E4M3
+           | (0u << 10)                               // B: E4M3
+           | (0u << 15)                               // A K-major
+           | ((b_mn_major ? 1u : 0u) << 16)           // B major-ness
+           | ((uint32_t)(N >> 3) << 17)               // N / 8
+           | (1u << 23)                               // scale factors: UE8M0
+           | ((uint32_t)(M >> 4) << 24)               // M / 16
+           | (0u << 29);                              // A scale-factor byte 0
+}
+
+// D[tmem] (+)= (A * sfA) x (B * sfB)^T with one UE8M0 scale per row of A and
+// per column of B for this 32-wide K step (kind::mxf8f6f4, scale_vec::1X).
+// Scale layout in tensor memory (M = 128): the scale of A row m sits in lane
+// m, column sfa + m/32; the scale of B column n in column sfb + n/32, lane
+// 32q + n%32 of every lane quarter q (one copy per quarter of D's rows).
+__device__ __forceinline__ void mma_mxf8f6f4(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
+                                             uint32_t sfa_tmem, uint32_t sfb_tmem, uint32_t accumulate)
+{
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %6, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::mxf8f6f4.block_scale.scale_vec::1X [%0], %1, %2, %3, [%4], [%5], p;\n\t}" ::"r"(d_tmem),
+        "l"(adesc), "l"(bdesc), "r"(idesc), "r"(sfa_tmem), "r"(sfb_tmem), "r"(accumulate)
+        : "memory");
+}
+
+// 32 lanes x 32 bits, 1 and 8 consecutive columns: thread i of the warp
+// writes lane (base lane + i).
+__device__ __forceinline__ void tmem_st_x1(uint32_t taddr, uint32_t v)
+{
+    asm volatile("tcgen05.st.sync.aligned.32x32b.x1.b32 [%0], {%1};" ::"r"(taddr), "r"(v) : "memory");
+}
+
+__device__ __forceinline__ void tmem_st_x8(uint32_t taddr, const uint32_t (&v)[8])
+{
+    asm volatile("tcgen05.st.sync.aligned.32x32b.x8.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8};" ::"r"(taddr), "r"(v[0]),
+                 "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7])
+                 : "memory");
+}
+
+__device__ __forceinline__ void tmem_wait_st()
+{
+    asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+}
+
 // ---------------------------------------------------------- conversions ----
 
 // Two FP32 values -> two E4M3 bytes (lo in the low byte), round to nearest

@@ -4,7 +4,9 @@
 // read, and 128x128 blocks (weights).
 //
 // The group rule (amax, s = amax/448, inv = 448/amax, one RNE saturating
-// conversion of x*inv) is in group_rule.cuh.
+// conversion of x*inv) is in group_rule.cuh, with its power-of-two variant
+// (s = the smallest 2^e with amax <= 448 * 2^e) that the *_pow2 entry points
+// select through the P2 template parameter.
 //
 // The kernels are streams bound by HBM and instruction issue (2 bytes read,
 // 1 byte + 4/128 or 4/16384 bytes written per element). They read with
@@ -45,7 +47,7 @@ __device__ __forceinline__ uint2 quant8(const uint4 &v, float inv)
 // patterns m[0..N) of its N groups (shuffle-reduced over the half-warp);
 // lane (16h + j) computes the scale pair of group j and the pairs are
 // broadcast back. Bit-identical to calling group_scale per group.
-template <int N>
+template <int N, bool P2>
 __device__ __forceinline__ void group_scales_batched(const uint32_t (&m)[N], float (&s)[N], float (&inv)[N])
 {
     static_assert(N <= 16, "one group per lane of a half-warp");
@@ -55,7 +57,7 @@ __device__ __forceinline__ void group_scales_batched(const uint32_t (&m)[N], flo
 #pragma unroll
     for (int i = 1; i < N; ++i)
         mine = j == i ? m[i] : mine;
-    const ScalePair sp = group_scale(__uint_as_float(mine << 16));
+    const ScalePair sp = group_scale_rule<P2>(__uint_as_float(mine << 16));
 #pragma unroll
     for (int i = 0; i < N; ++i) {
         s[i] = __shfl_sync(0xffffffffu, sp.s, (lane & 16) + i);
@@ -88,7 +90,7 @@ constexpr int QR_ITEMS = QR_ROWS * QR_GROUPS / 16;
 // MoE expert order); an index outside [0, n_src) is reported as
 // FP8FG_EDEVICE in the status word and reads source row 0. Quantisation is
 // per row, so the result equals gathering the rows of the plain output.
-template <bool GATHER>
+template <bool GATHER, bool P2>
 __global__ void __launch_bounds__(256, 8) quant_rows_kernel(const uint16_t *__restrict__ x, int64_t rows,
                                                             int64_t ngroups, int64_t ldx, uint8_t *__restrict__ q,
                                                             int64_t ldq, float *__restrict__ scales, int64_t ld_s,
@@ -132,7 +134,7 @@ __global__ void __launch_bounds__(256, 8) quant_rows_kernel(const uint16_t *__re
             m[i] = max(m[i], __shfl_xor_sync(0xffffffffu, m[i], off));
     }
     float sc[QR_ITEMS], inv[QR_ITEMS];
-    group_scales_batched<QR_ITEMS>(m, sc, inv);
+    group_scales_batched<QR_ITEMS, P2>(m, sc, inv);
 #pragma unroll
     for (int i = 0; i < QR_ITEMS; ++i) {
         if (g_ok && r0 + i < rows) {
@@ -157,6 +159,7 @@ __global__ void __launch_bounds__(256, 8) quant_rows_kernel(const uint16_t *__re
 // the transposed output.
 constexpr int QT_COLS = 64;
 
+template <bool P2>
 __global__ void __launch_bounds__(256, 8) quant_cols_t_kernel(const uint16_t *__restrict__ x, int64_t rows,
                                                            int64_t cols, int64_t ldx, uint8_t *__restrict__ qT,
                                                            int64_t ldq, float *__restrict__ scales, int64_t ld_s)
@@ -192,7 +195,7 @@ __global__ void __launch_bounds__(256, 8) quant_cols_t_kernel(const uint16_t *__
     s_amax[part][c] = m;
     __syncthreads();
     m = max(max(s_amax[0][c], s_amax[1][c]), max(s_amax[2][c], s_amax[3][c]));
-    const ScalePair sp = group_scale(__uint_as_float(m << 16));
+    const ScalePair sp = group_scale_rule<P2>(__uint_as_float(m << 16));
     const int64_t col = c0 + c;
     if (col < cols) {
         uint32_t packed[8];
@@ -220,6 +223,7 @@ __global__ void __launch_bounds__(256, 8) quant_cols_t_kernel(const uint16_t *__
 // its columns from a shared-memory copy. The outputs are bit-identical to
 // fp8_quant_1x128 with transpose 0 and 1 (same group rule, same products).
 // 4.06 bytes of traffic per element instead of 2 x 3.03.
+template <bool P2>
 __global__ void __launch_bounds__(256, 5) quant_dual_kernel(const uint16_t *__restrict__ x, int64_t ldx,
                                                             uint8_t *__restrict__ q, int64_t ldq,
                                                             float *__restrict__ scales, int64_t ld_s,
@@ -251,7 +255,7 @@ __global__ void __launch_bounds__(256, 5) quant_dual_kernel(const uint16_t *__re
             mr[i] = max(mr[i], __shfl_xor_sync(0xffffffffu, mr[i], off));
     }
     float sr[8], ir[8];
-    group_scales_batched<8>(mr, sr, ir);
+    group_scales_batched<8, P2>(mr, sr, ir);
 #pragma unroll
     for (int i = 0; i < 8; ++i) {
         const int rr = i * 16 + (tid >> 4);
@@ -272,7 +276,7 @@ __global__ void __launch_bounds__(256, 5) quant_dual_kernel(const uint16_t *__re
     s_amax[part][c] = m;
     __syncthreads();
     m = max(s_amax[0][c], s_amax[1][c]);
-    const ScalePair sp = group_scale(__uint_as_float(m << 16));
+    const ScalePair sp = group_scale_rule<P2>(__uint_as_float(m << 16));
     const int64_t col = c0 + c;
     uint4 *dst = reinterpret_cast<uint4 *>(qT + col * ldqT + r0 + part * 64);
 #pragma unroll
@@ -295,6 +299,7 @@ __global__ void __launch_bounds__(256, 5) quant_dual_kernel(const uint16_t *__re
 
 // ------------------------------------------------------- 128x128 blocks ----
 // One CTA per block: 256 threads x 8 chunks of 8 bf16 held in registers.
+template <bool P2>
 __global__ void __launch_bounds__(256) quant_blocks_kernel(const uint16_t *__restrict__ w, int64_t K, int64_t ldw,
                                                            uint8_t *__restrict__ q, int64_t ldq,
                                                            float *__restrict__ scales)
@@ -324,7 +329,7 @@ __global__ void __launch_bounds__(256) quant_blocks_kernel(const uint16_t *__res
 #pragma unroll
     for (int i = 1; i < 8; ++i)
         m = max(m, s_warp[i]);
-    const ScalePair sp = group_scale(__uint_as_float(m << 16));
+    const ScalePair sp = group_scale_rule<P2>(__uint_as_float(m << 16));
     uint8_t *dst = q + bi * GROUP * ldq + bj * GROUP;
 #pragma unroll
     for (int i = 0; i < 8; ++i) {
@@ -335,12 +340,12 @@ __global__ void __launch_bounds__(256) quant_blocks_kernel(const uint16_t *__res
         scales[bi * (K / GROUP) + bj] = sp.s;
 }
 
-}  // namespace
-}  // namespace fp8fg
+// ----------------------------------------------------------- entry points ----
+// Argument checks and launches, shared by the pages' rule (P2 = false) and
+// the power-of-two variant.
 
-using namespace fp8fg;
-
-extern "C" int fp8_quant_1x128(const void *x, int64_t rows, int64_t cols, int64_t ldx, uint8_t *q, int64_t ldq,
+template <bool P2>
+int quant_1x128(const void *x, int64_t rows, int64_t cols, int64_t ldx, uint8_t *q, int64_t ldq,
                                float *scales, int64_t ld_s, int transpose, void *stream)
 {
     if (rows < 0 || cols < 0 || (transpose != 0 && transpose != 1))
@@ -367,20 +372,21 @@ extern "C" int fp8_quant_1x128(const void *x, int64_t rows, int64_t cols, int64_
         const int64_t tiles = tiles_g * ((rows + QR_ROWS - 1) / QR_ROWS);
         if (tiles > 0x7FFFFFFF)
             return FP8FG_EINVAL;
-        quant_rows_kernel<false><<<(unsigned)tiles, 256, 0, s>>>(static_cast<const uint16_t *>(x), rows, ngroups,
+        quant_rows_kernel<false, P2><<<(unsigned)tiles, 256, 0, s>>>(static_cast<const uint16_t *>(x), rows, ngroups,
                                                                   ldx, q, ldq, scales, ld_s, tiles_g, nullptr, 0,
                                                                   nullptr);
     } else {
         const int64_t gx = (cols + QT_COLS - 1) / QT_COLS, gy = rows / GROUP;
         if (gx > 0x7FFFFFFF || gy > 65535)
             return FP8FG_EINVAL;
-        quant_cols_t_kernel<<<dim3((unsigned)gx, (unsigned)gy), 256, 0, s>>>(
+        quant_cols_t_kernel<P2><<<dim3((unsigned)gx, (unsigned)gy), 256, 0, s>>>(
             static_cast<const uint16_t *>(x), rows, cols, ldx, q, ldq, scales, ld_s);
     }
     return launch_status();
 }
 
-extern "C" int fp8_quant_1x128_gather(const void *x, int64_t n_src, int64_t cols, int64_t ldx,
+template <bool P2>
+int quant_1x128_gather(const void *x, int64_t n_src, int64_t cols, int64_t ldx,
                                       const int32_t *row_index, int64_t rows, uint8_t *q, int64_t ldq, float *scales,
                                       int64_t ld_s, void *stream)
 {
@@ -402,13 +408,14 @@ extern "C" int fp8_quant_1x128_gather(const void *x, int64_t n_src, int64_t cols
     const int64_t tiles = tiles_g * ((rows + QR_ROWS - 1) / QR_ROWS);
     if (tiles > 0x7FFFFFFF)
         return FP8FG_EINVAL;
-    quant_rows_kernel<true><<<(unsigned)tiles, 256, 0, static_cast<cudaStream_t>(stream)>>>(
+    quant_rows_kernel<true, P2><<<(unsigned)tiles, 256, 0, static_cast<cudaStream_t>(stream)>>>(
         static_cast<const uint16_t *>(x), rows, ngroups, ldx, q, ldq, scales, ld_s, tiles_g, row_index, n_src,
         status);
     return launch_status();
 }
 
-extern "C" int fp8_quant_1x128_dual(const void *x, int64_t rows, int64_t cols, int64_t ldx, uint8_t *q,
+template <bool P2>
+int quant_1x128_dual(const void *x, int64_t rows, int64_t cols, int64_t ldx, uint8_t *q,
                                     int64_t ldq, float *scales, int64_t ld_s, uint8_t *qT, int64_t ldqT,
                                     float *scalesT, int64_t ld_sT, void *stream)
 {
@@ -427,12 +434,13 @@ extern "C" int fp8_quant_1x128_dual(const void *x, int64_t rows, int64_t cols, i
     const int64_t gx = cols / GROUP, gy = rows / GROUP;
     if (gx > 0x7FFFFFFF || gy > 65535)
         return FP8FG_EINVAL;
-    quant_dual_kernel<<<dim3((unsigned)gx, (unsigned)gy), 256, 0, static_cast<cudaStream_t>(stream)>>>(
+    quant_dual_kernel<P2><<<dim3((unsigned)gx, (unsigned)gy), 256, 0, static_cast<cudaStream_t>(stream)>>>(
         static_cast<const uint16_t *>(x), ldx, q, ldq, scales, ld_s, qT, ldqT, scalesT, ld_sT);
     return launch_status();
 }
 
-extern "C" int fp8_quant_128x128(const void *w, int64_t N, int64_t K, int64_t ldw, uint8_t *q, int64_t ldq,
+template <bool P2>
+int quant_128x128(const void *w, int64_t N, int64_t K, int64_t ldw, uint8_t *q, int64_t ldq,
                                  float *scales, void *stream)
 {
     if (N < 0 || K < 0 || N % GROUP != 0 || K % GROUP != 0 || ldw < K || ldq < K)
@@ -449,7 +457,64 @@ extern "C" int fp8_quant_128x128(const void *w, int64_t N, int64_t K, int64_t ld
     const int64_t gx = K / GROUP, gy = N / GROUP;
     if (gx > 0x7FFFFFFF || gy > 65535)
         return FP8FG_EINVAL;
-    quant_blocks_kernel<<<dim3((unsigned)gx, (unsigned)gy), 256, 0, static_cast<cudaStream_t>(stream)>>>(
+    quant_blocks_kernel<P2><<<dim3((unsigned)gx, (unsigned)gy), 256, 0, static_cast<cudaStream_t>(stream)>>>(
         static_cast<const uint16_t *>(w), K, ldw, q, ldq, scales);
     return launch_status();
+}
+
+}  // namespace
+}  // namespace fp8fg
+
+using namespace fp8fg;
+
+extern "C" int fp8_quant_1x128(const void *x, int64_t rows, int64_t cols, int64_t ldx, uint8_t *q, int64_t ldq,
+                               float *scales, int64_t ld_s, int transpose, void *stream)
+{
+    return quant_1x128<false>(x, rows, cols, ldx, q, ldq, scales, ld_s, transpose, stream);
+}
+
+extern "C" int fp8_quant_1x128_gather(const void *x, int64_t n_src, int64_t cols, int64_t ldx,
+                                      const int32_t *row_index, int64_t rows, uint8_t *q, int64_t ldq, float *scales,
+                                      int64_t ld_s, void *stream)
+{
+    return quant_1x128_gather<false>(x, n_src, cols, ldx, row_index, rows, q, ldq, scales, ld_s, stream);
+}
+
+extern "C" int fp8_quant_1x128_dual(const void *x, int64_t rows, int64_t cols, int64_t ldx, uint8_t *q,
+                                    int64_t ldq, float *scales, int64_t ld_s, uint8_t *qT, int64_t ldqT,
+                                    float *scalesT, int64_t ld_sT, void *stream)
+{
+    return quant_1x128_dual<false>(x, rows, cols, ldx, q, ldq, scales, ld_s, qT, ldqT, scalesT, ld_sT, stream);
+}
+
+extern "C" int fp8_quant_128x128(const void *w, int64_t N, int64_t K, int64_t ldw, uint8_t *q, int64_t ldq,
+                                 float *scales, void *stream)
+{
+    return quant_128x128<false>(w, N, K, ldw, q, ldq, scales, stream);
+}
+
+extern "C" int fp8_quant_1x128_pow2(const void *x, int64_t rows, int64_t cols, int64_t ldx, uint8_t *q, int64_t ldq,
+                                    float *scales, int64_t ld_s, int transpose, void *stream)
+{
+    return quant_1x128<true>(x, rows, cols, ldx, q, ldq, scales, ld_s, transpose, stream);
+}
+
+extern "C" int fp8_quant_1x128_gather_pow2(const void *x, int64_t n_src, int64_t cols, int64_t ldx,
+                                           const int32_t *row_index, int64_t rows, uint8_t *q, int64_t ldq,
+                                           float *scales, int64_t ld_s, void *stream)
+{
+    return quant_1x128_gather<true>(x, n_src, cols, ldx, row_index, rows, q, ldq, scales, ld_s, stream);
+}
+
+extern "C" int fp8_quant_1x128_dual_pow2(const void *x, int64_t rows, int64_t cols, int64_t ldx, uint8_t *q,
+                                         int64_t ldq, float *scales, int64_t ld_s, uint8_t *qT, int64_t ldqT,
+                                         float *scalesT, int64_t ld_sT, void *stream)
+{
+    return quant_1x128_dual<true>(x, rows, cols, ldx, q, ldq, scales, ld_s, qT, ldqT, scalesT, ld_sT, stream);
+}
+
+extern "C" int fp8_quant_128x128_pow2(const void *w, int64_t N, int64_t K, int64_t ldw, uint8_t *q, int64_t ldq,
+                                      float *scales, void *stream)
+{
+    return quant_128x128<true>(w, N, K, ldw, q, ldq, scales, stream);
 }

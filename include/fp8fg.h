@@ -269,6 +269,62 @@ FP8FG_API int fp8_grouped_gemm(const uint8_t *Xq, const float *sX, int64_t ld_sX
                      void *Y, int out, int64_t ldy, void *stream);
 
 /* ---------------------------------------------------------------------
+ * Microscaling variant: power-of-two group scales and the tensor cores'
+ * own block scaling.
+ * Source: innerforce.co.kr, the paragraph relating the fine-grained groups
+ * to microscaling formats, which Blackwell tensor cores support; tonho.wtf
+ * "o que isso custou" (MMA with group scaling on the hardware wish list) and
+ * "onde isso aparece hoje" (microscaling announced for Blackwell).
+ * Microscaling shares a power-of-two scale per group; the pages give no
+ * rounding for it. Reading used here: the groups stay the pages' (1x128,
+ * 128x1, 128x128) and
+ *   scale   s = 2^e, the smallest power of two with amax <= 448 * 2^e,
+ *           e >= -127 (the UE8M0 range); amax == 0 gives s = 1. inv = 2^-e.
+ *   code    q = E4M3(x * inv), one rounding (x * inv is exact), never
+ *           saturating since |x * inv| <= 448.
+ * Scales are stored as FP32 values (exact powers of two) in the same layouts
+ * as the entry points above, so either GEMM accepts them.
+ *
+ * fp8_quant_1x128_pow2, fp8_quant_1x128_dual_pow2,
+ * fp8_quant_1x128_gather_pow2, fp8_quant_128x128_pow2: arguments, layouts,
+ * alignment and errors exactly as fp8_quant_1x128, fp8_quant_1x128_dual,
+ * fp8_quant_1x128_gather and fp8_quant_128x128; only the scale rule differs.
+ * ------------------------------------------------------------------- */
+FP8FG_API int fp8_quant_1x128_pow2(const void *x, int64_t rows, int64_t cols, int64_t ldx,
+                         uint8_t *q, int64_t ldq, float *scales, int64_t ld_s,
+                         int transpose, void *stream);
+FP8FG_API int fp8_quant_1x128_dual_pow2(const void *x, int64_t rows, int64_t cols, int64_t ldx,
+                         uint8_t *q, int64_t ldq, float *scales, int64_t ld_s,
+                         uint8_t *qT, int64_t ldqT, float *scalesT, int64_t ld_sT,
+                         void *stream);
+FP8FG_API int fp8_quant_1x128_gather_pow2(const void *x, int64_t n_src, int64_t cols, int64_t ldx,
+                         const int32_t *row_index, int64_t rows,
+                         uint8_t *q, int64_t ldq, float *scales, int64_t ld_s, void *stream);
+FP8FG_API int fp8_quant_128x128_pow2(const void *w, int64_t N, int64_t K, int64_t ldw,
+                         uint8_t *q, int64_t ldq, float *scales, void *stream);
+
+/* ---------------------------------------------------------------------
+ * fp8_gemm_mx: the GEMM of fp8_gemm_blockscaled (same modes, operands,
+ * layouts, alignment and errors) for power-of-two scales, with the scales
+ * applied inside the tensor cores' block-scaled MMA (one UE8M0 scale per
+ * A row and per B column for every 32-wide contraction step; a 128-wide
+ * group repeats its scale over its four steps). The whole contraction
+ * accumulates in FP32 in tensor memory; there is no per-block promotion.
+ * Mathematically C is the same sum as fp8_gemm_blockscaled computes:
+ *     C[i,j] = sum_kb sA(i,kb) sB(j,kb) P(i,j,kb),
+ * rounded differently (the tolerance is the same).
+ *   Every scale must be a power of two in [2^-127, 2^127] (the *_pow2
+ *   quantisers write only such values); a scale's FP32 exponent field is
+ *   what the tensor cores receive, so other values are taken as the power
+ *   of two at or below them.
+ * ------------------------------------------------------------------- */
+FP8FG_API int fp8_gemm_mx(int mode,
+                         const uint8_t *A, const float *sA, int64_t lda, int64_t ld_sA,
+                         const uint8_t *B, const float *sB, int64_t ldb, int64_t ld_sB,
+                         int64_t M, int64_t N, int64_t K,
+                         void *C, int out, int64_t ldc, void *stream);
+
+/* ---------------------------------------------------------------------
  * Status and diagnostics (no counterpart on the pages).
  * ------------------------------------------------------------------- */
 
@@ -283,8 +339,9 @@ FP8FG_API int fp8fg_device_status(void *stream);
 /* Library version (major*10000 + minor*100 + patch). */
 FP8FG_API int fp8fg_version(void);
 
-/* Test hook: when `skip` != 0, the next fp8_gemm_blockscaled launch on the
- * current device withholds its first operand load, so the consumers' bounded
+/* Test hook: when `skip` != 0, the next fp8_gemm_blockscaled or fp8_gemm_mx
+ * launch on the current device withholds its first operand load (a
+ * fp8_grouped_gemm launch clears the request without using it), so the consumers' bounded
  * waits run out and the launch reports FP8FG_ETIMEOUT. One-shot; returns
  * FP8FG_OK. For exercising failure detection without a GPU fault. */
 FP8FG_API int fp8fg_test_skip_first_load(int skip);
