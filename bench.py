@@ -22,7 +22,7 @@ Other workloads, one JSON line each, for the remaining kernels:
     tiny      128 x 256 x 128 fprop, FP32 out (latency)
     dense_e4m3  the dense step with the GEMM's output quantised 1x128 in its
               epilogue
-    dense_mx, trio_mx  the dense and trio steps in the microscaling variant:
+    dense_mx, trio_mx, moe_mx  the dense, trio and MoE steps in the microscaling variant:
               power-of-two group scales, GEMMs on the tensor cores'
               block-scaled MMA (no per-block promotion)
 
@@ -32,7 +32,7 @@ dirty lines are written back inside the next step), outside the events.
 
 Usage:
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
-                    [--workload dense|trio|moe|outliers|tiny|dense_e4m3|dense_mx|trio_mx]
+                    [--workload dense|trio|moe|outliers|tiny|dense_e4m3|dense_mx|trio_mx|moe_mx]
 Under torchrun (N > 1) every rank runs its own replica of the workload
 (weak scaling, no data-path collective); times are the max over ranks.
 ``--impl reference`` times the CPU oracle on a bounded sample of the same
@@ -68,6 +68,8 @@ WORKLOADS = {
                   "next layer's input): quant X 1x128 + GEMM, M=4096 K=7168 N=7168",
     "dense_mx": "dense projection fprop, microscaling variant (power-of-two scales, tensor-core block "
                 "scaling): quant 1x128 + GEMM, M=4096 K=7168 N=7168, bf16 out",
+    "moe_mx": "MoE experts, microscaling variant (power-of-two scales, tensor-core block scaling): 4096 tokens, "
+              "256 experts 2048x7168, top-8 with Zipf(1.1) bias; quant X into expert order + grouped GEMM",
     "trio_mx": "linear 7168->18432 at M=8192, microscaling variant (power-of-two scales, tensor-core block "
                "scaling): quant W 128x128, X/dY 1x128 and transposed; fprop, dgrad, wgrad",
 }
@@ -269,7 +271,7 @@ def build(workload, dev, seed, fg, synth):
         g.manual_seed(seed + 1)
         for e in range(E):
             we = (torch.randn(Nw, Kx, generator=g, device=dev) * 0.02).to(torch.bfloat16)
-            fg.fp8_quant_128x128(we, q=wq[e], scales=sw[e])
+            fg.fp8_quant_128x128(we, q=wq[e], scales=sw[e], pow2=mx)
         T = mo.x.shape[0]
         R = int(mo.expert_offsets[-1].item())
         # the routed rows are quantised straight into expert order (the
@@ -282,10 +284,11 @@ def build(workload, dev, seed, fg, synth):
         f = 2.0 * R * Nw * Kx
         parts = [
             Part("quant_x_gather", "quant_rows_kernel<gather>",
-                 lambda: fg.fp8_quant_1x128_gather(mo.x, mo.row_index, q=xg, scales=sxg), "hbm",
+                 lambda: fg.fp8_quant_1x128_gather(mo.x, mo.row_index, q=xg, scales=sxg, pow2=mx), "hbm",
                  2 * T * Kx + (Q1X128_B - 2) * R * Kx + 4 * R),
-            Part("grouped", "gemm_kernel<GROUPED>",
-                 lambda: fg.fp8_grouped_gemm(xg, sxg, None, mo.expert_offsets, wq, sw, R, y=y), "tensor",
+            Part("grouped", "gemm_mx_kernel<GROUPED_C>" if mx else "gemm_kernel<GROUPED_C>",
+                 (lambda: fg.fp8_grouped_gemm_mx(xg, sxg, mo.expert_offsets, wq, sw, R, y=y)) if mx else
+                 (lambda: fg.fp8_grouped_gemm(xg, sxg, None, mo.expert_offsets, wq, sw, R, y=y)), "tensor",
                  f, extra_bytes=moved),
         ]
         cnt = mo.counts.cpu()
@@ -518,7 +521,7 @@ def oracle_dims(workload):
     """(M, K, N) of the workload's first GEMM, the one the CPU sample runs."""
     return {"dense": (4096, 7168, 7168), "dense_e4m3": (4096, 7168, 7168), "outliers": (16384, 7168, 7168),
             "trio": (8192, 7168, 18432), "moe": (32768, 7168, 2048), "tiny": (128, 256, 128),
-            "dense_mx": (4096, 7168, 7168), "trio_mx": (8192, 7168, 18432)}[workload]
+            "dense_mx": (4096, 7168, 7168), "trio_mx": (8192, 7168, 18432), "moe_mx": (32768, 7168, 2048)}[workload]
 
 
 def cpu_sample(workload, rows, seed=0):

@@ -50,6 +50,7 @@ def lib():
         L.fp8_quant_1x128_dual_pow2.argtypes = L.fp8_quant_1x128_dual.argtypes
         L.fp8_quant_128x128_pow2.argtypes = L.fp8_quant_128x128.argtypes
         L.fp8_gemm_mx.argtypes = [I32, P, P, I64, I64, P, P, I64, I64, I64, I64, I64, P, I32, I64, P]
+        L.fp8_grouped_gemm_mx.argtypes = [P, P, I64, P, ctypes.c_int32, I64, P, P, I64, I64, P, I32, I64, P]
         L.fp8_gemm_blockscaled.argtypes = [I32, P, P, I64, I64, P, P, I64, I64, I64, I64, I64, P, I32, I64, P]
         L.fp8_gemm_blockscaled_e4m3.argtypes = [I32, P, P, I64, I64, P, P, I64, I64, I64, I64, I64, P, I64, P, I64, P]
         L.fp8_grouped_gemm.argtypes = [P, P, I64, I64, P, P, ctypes.c_int32, I64, P, P, I64, I64, P, I32, I64, P]
@@ -331,6 +332,27 @@ def fp8_grouped_gemm(xq, sx, row_index, expert_offsets, wq, sw, n_rows, out_dtyp
                                 n_rows, _ptr(wq), _ptr(sw), N, K, _ptr(y), _out_code(y.dtype), y.stride(0),
                                 _stream(stream))
     _check(rc, "fp8_grouped_gemm")
+    return y
+
+
+def fp8_grouped_gemm_mx(xq, sx, expert_offsets, wq, sw, n_rows, out_dtype=None, y=None, stream=None):
+    """fp8_grouped_gemm with rows already in expert order (row_index=None)
+    for power-of-two scales, on the tensor cores' block-scaled MMA."""
+    torch = _torch()
+    for t, n in ((xq, "xq"), (sx, "sx"), (wq, "wq"), (sw, "sw")):
+        if not t.is_contiguous() and n != "sx":
+            raise ValueError(n + " must be contiguous")
+    if expert_offsets.dtype != torch.int32 or not expert_offsets.is_contiguous():
+        raise ValueError("expert_offsets must be contiguous int32")
+    E, N, K = wq.shape
+    if out_dtype is None:
+        out_dtype = torch.bfloat16
+    if y is None:
+        y = torch.empty((n_rows, N), dtype=out_dtype, device=xq.device)
+    _rowmajor(y, "y")
+    rc = lib().fp8_grouped_gemm_mx(_ptr(xq), _ptr(sx), sx.stride(0), _ptr(expert_offsets), E, n_rows, _ptr(wq),
+                                   _ptr(sw), N, K, _ptr(y), _out_code(y.dtype), y.stride(0), _stream(stream))
+    _check(rc, "fp8_grouped_gemm_mx")
     return y
 
 

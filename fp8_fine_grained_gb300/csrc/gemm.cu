@@ -35,6 +35,7 @@
 #include <cuda_bf16.h>
 
 #include "group_rule.cuh"
+#include "group_tiles.cuh"
 #include "host_common.h"
 #include "ptx.cuh"
 #include "tensor_map.h"
@@ -138,37 +139,16 @@ struct Tile {
     int expert;
 };
 
-__device__ __forceinline__ int64_t grouped_total_tiles(const int32_t *prefix, int n_experts)
-{
-    return prefix[n_experts];
-}
-
 template <int MODE>
 __device__ __forceinline__ Tile decode_tile(int64_t t, const Params &p, const int32_t *prefix)
 {
     Tile tl;
     if constexpr (is_grouped(MODE)) {
-        // experts are laid out in the tile space one after the other; within
-        // an expert the m-tiles vary fastest, so CTAs running together share
-        // the expert's weight tiles in L2.
-        int lo = 0, hi = p.n_experts;  // find last e with prefix[e] <= t
-        while (hi - lo > 1) {
-            int mid = (lo + hi) >> 1;
-            if (prefix[mid] <= t)
-                lo = mid;
-            else
-                hi = mid;
-        }
-        const int e = lo;
-        const int64_t local = t - prefix[e];
-        int64_t r0 = p.expert_offsets[e], r1 = p.expert_offsets[e + 1];
-        r0 = r0 < 0 ? 0 : (r0 > p.n_rows ? p.n_rows : r0);
-        r1 = r1 > p.n_rows ? p.n_rows : r1;
-        const int64_t mt = (r1 - r0 + BM - 1) / BM;
-        tl.expert = e;
-        tl.m0 = r0 + (local % mt) * BM;
-        tl.row_end = r1;
-        tl.n0 = (local / mt) * BN;
+        const GroupTile g = decode_group_tile(t, prefix, p.expert_offsets, p.n_experts, p.n_rows, BM, BN);
+        tl.expert = g.expert;
+        tl.m0 = g.m0;
+        tl.row_end = g.row_end;
+        tl.n0 = g.n0;
     } else {
         // bands of 16 m-tiles, m fastest inside a band: CTAs running at the
         // same time read ~16 A tiles and ~10 B tiles, all L2-resident.
@@ -183,58 +163,6 @@ __device__ __forceinline__ Tile decode_tile(int64_t t, const Params &p, const in
         tl.expert = 0;
     }
     return tl;
-}
-
-// Block-wide exclusive prefix over experts of (m-tiles x n-tiles); flags
-// malformed offsets. Runs once per CTA at kernel start.
-__device__ void build_group_prefix(const Params &p, int32_t *prefix)
-{
-    __shared__ int32_t warp_sums[NUM_THREADS / 32];
-    const int E = p.n_experts;
-    const int per = (E + NUM_THREADS - 1) / NUM_THREADS;
-    const int e0 = threadIdx.x * per;
-    int32_t local[16];  // per <= 4096/320 + 1 = 13
-    int32_t sum = 0;
-    for (int i = 0; i < per && i < 16; ++i) {
-        const int e = e0 + i;
-        int32_t v = 0;
-        if (e < E) {
-            int64_t r0 = p.expert_offsets[e], r1 = p.expert_offsets[e + 1];
-            if (r0 < 0 || r1 < r0 || r1 > p.n_rows)
-                atomicCAS(p.status, 0, FP8FG_EDEVICE);
-            r0 = r0 < 0 ? 0 : (r0 > p.n_rows ? p.n_rows : r0);
-            r1 = r1 > p.n_rows ? p.n_rows : r1;
-            const int64_t m = r1 > r0 ? r1 - r0 : 0;
-            v = (int32_t)(((m + BM - 1) / BM) * p.num_n_tiles);
-        }
-        local[i] = v;
-        sum += v;
-    }
-    // inclusive scan of per-thread sums
-    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-    int32_t x = sum;
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-        int32_t y = __shfl_up_sync(0xffffffffu, x, o);
-        if (lane >= o)
-            x += y;
-    }
-    if (lane == 31)
-        warp_sums[warp] = x;
-    __syncthreads();
-    int32_t base = 0;
-    for (int w = 0; w < warp; ++w)
-        base += warp_sums[w];
-    int32_t run = base + x - sum;  // exclusive prefix of this thread
-    for (int i = 0; i < per && i < 16; ++i) {
-        const int e = e0 + i;
-        if (e < E)
-            prefix[e] = run;
-        run += local[i];
-    }
-    if (threadIdx.x == NUM_THREADS - 1)
-        prefix[E] = run;  // total (last thread's run ends at the grand total)
-    __syncthreads();
 }
 
 template <int MODE, int OUT>
@@ -278,14 +206,14 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         tmem_relinquish();
     }
     if constexpr (is_grouped(MODE))
-        build_group_prefix(p, prefix);
+        build_group_prefix<NUM_THREADS>(p.expert_offsets, p.n_experts, p.n_rows, p.num_n_tiles, BM, p.status, prefix);
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem_base = *tmem_ptr;
 
     const int64_t num_tiles =
-        is_grouped(MODE) ? (int64_t)grouped_total_tiles(prefix, p.n_experts) : p.num_m_tiles * p.num_n_tiles;
+        is_grouped(MODE) ? (int64_t)prefix[p.n_experts] : p.num_m_tiles * p.num_n_tiles;
     const int num_kb = (int)(p.K / BK);
 
     if (warp == 0) {

@@ -36,6 +36,7 @@
 // roles leave their loops, drain their in-flight work and free TMEM.
 #include <cuda_bf16.h>
 
+#include "group_tiles.cuh"
 #include "host_common.h"
 #include "ptx.cuh"
 #include "tensor_map.h"
@@ -69,7 +70,10 @@ constexpr int SF_SLOTS = 4;
 constexpr uint32_t STAGE_C_BYTES = 32 * 64;
 static_assert(SF_COL0 + SF_SLOTS * SF_SLOT_COLS <= TMEM_COLS, "scale slots inside the allocation");
 
-enum Mode { FPROP = 0, DGRAD = 1, WGRAD = 2 };
+// GROUPED_C: MoE experts over rows already in expert order (as the gather
+// quantiser writes them); B is the experts' weights [E][N][K].
+enum Mode { FPROP = 0, DGRAD = 1, WGRAD = 2, GROUPED_C = 3 };
+constexpr int MAX_EXPERTS = 4096;
 enum Out { OUT_F32 = 0, OUT_BF16 = 1 };
 
 struct Params {
@@ -84,6 +88,10 @@ struct Params {
     int *status;
     uint64_t wait_limit_ns;
     int skip_first_load;
+    // grouped mode
+    const int32_t *expert_offsets;
+    int n_experts;
+    int64_t n_rows;
 };
 
 struct SmemLayout {
@@ -98,21 +106,31 @@ struct SmemLayout {
     static constexpr uint32_t tmem_ptr_off = tempty_off + 8;
     static constexpr uint32_t abort_off = tmem_ptr_off + 4;
     static constexpr uint32_t stage_c_off = (abort_off + 4 + 15) & ~15u;
-    static constexpr uint32_t total = stage_c_off + EPI_WARPS * STAGE_C_BYTES + 1024;  // + alignment slack
+    static constexpr uint32_t prefix_off = stage_c_off + EPI_WARPS * STAGE_C_BYTES;  // grouped: tile prefix
+    static constexpr uint32_t total = prefix_off + 4 * (MAX_EXPERTS + 1) + 1024;     // + alignment slack
 };
 static_assert(SmemLayout::total <= 232448, "shared memory budget");
 
-// Bands of 16 m-tiles, m fastest inside a band (A and B tiles of CTAs that
-// run together stay in L2).
-__device__ __forceinline__ void decode_tile(int64_t t, const Params &p, int64_t &m0, int64_t &n0)
+// Dense modes: bands of 16 m-tiles, m fastest inside a band (A and B tiles
+// of CTAs that run together stay in L2). Grouped: the experts' tiles.
+template <int MODE>
+__device__ __forceinline__ GroupTile decode_tile(int64_t t, const Params &p, const int32_t *prefix)
 {
-    constexpr int64_t BAND = 16;
-    const int64_t per_band = BAND * p.num_n_tiles;
-    const int64_t band = t / per_band, r = t % per_band;
-    const int64_t mfirst = band * BAND;
-    const int64_t gm = (p.num_m_tiles - mfirst) < BAND ? (p.num_m_tiles - mfirst) : BAND;
-    m0 = (mfirst + r % gm) * BM;
-    n0 = (r / gm) * BN;
+    if constexpr (MODE == GROUPED_C) {
+        return decode_group_tile(t, prefix, p.expert_offsets, p.n_experts, p.n_rows, BM, BN);
+    } else {
+        constexpr int64_t BAND = 16;
+        const int64_t per_band = BAND * p.num_n_tiles;
+        const int64_t band = t / per_band, r = t % per_band;
+        const int64_t mfirst = band * BAND;
+        const int64_t gm = (p.num_m_tiles - mfirst) < BAND ? (p.num_m_tiles - mfirst) : BAND;
+        GroupTile g;
+        g.m0 = (mfirst + r % gm) * BM;
+        g.n0 = (r / gm) * BN;
+        g.row_end = p.M;
+        g.expert = 0;
+        return g;
+    }
 }
 
 // UE8M0 byte of a power-of-two scale: its biased FP32 exponent (2^-127, an
@@ -137,6 +155,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     const uint32_t tempty_bar = sbase + SmemLayout::tempty_off;
     volatile uint32_t *tmem_ptr = reinterpret_cast<volatile uint32_t *>(smem + SmemLayout::tmem_ptr_off);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + SmemLayout::abort_off);
+    int32_t *prefix = reinterpret_cast<int32_t *>(smem + SmemLayout::prefix_off);
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
@@ -162,12 +181,14 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         tmem_alloc(sbase + SmemLayout::tmem_ptr_off, TMEM_COLS);
         tmem_relinquish();
     }
+    if constexpr (MODE == GROUPED_C)
+        build_group_prefix<NUM_THREADS>(p.expert_offsets, p.n_experts, p.n_rows, p.num_n_tiles, BM, p.status, prefix);
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem_base = *tmem_ptr;
 
-    const int64_t num_tiles = p.num_m_tiles * p.num_n_tiles;
+    const int64_t num_tiles = MODE == GROUPED_C ? (int64_t)prefix[p.n_experts] : p.num_m_tiles * p.num_n_tiles;
     const int num_kb = (int)(p.K / BK);
     // this CTA's blocks, counted over its tiles in order
     const int64_t my_tiles = num_tiles > blockIdx.x ? (num_tiles - blockIdx.x + gridDim.x - 1) / gridDim.x : 0;
@@ -180,8 +201,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         bool skip = p.skip_first_load && blockIdx.x == 0;
         bool ok = true;
         for (int64_t t = blockIdx.x; t < num_tiles && ok; t += gridDim.x) {
-            int64_t m0, n0;
-            decode_tile(t, p, m0, n0);
+            const GroupTile tl = decode_tile<MODE>(t, p, prefix);
+            const int64_t m0 = tl.m0, n0 = tl.n0;
+            const int64_t brow0 = MODE == GROUPED_C ? (int64_t)tl.expert * p.N + n0 : n0;  // first B row
             for (int kb = 0; kb < num_kb; ++kb) {
                 bool got = true;
                 if (lane == 0)
@@ -215,7 +237,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                         if (second_half)
                             tma_load_2d(b_dst + B_STAGE_BYTES / 2, &tmB, (int32_t)n0 + 128, kb * BK, fb);
                     } else {
-                        tma_load_2d(b_dst, &tmB, kb * BK, (int32_t)n0, fb);
+                        tma_load_2d(b_dst, &tmB, kb * BK, (int32_t)brow0, fb);
                     }
                 }
                 __syncwarp();
@@ -324,10 +346,18 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         struct Sf {
             float a, b[NB];
         };
-        int64_t ct = blockIdx.x, cm0 = 0, cn0 = 0;  // cursor: tile, its origin, block
-        int ckb = 0;
-        if (ct < num_tiles)
-            decode_tile(ct, p, cm0, cn0);
+        int64_t ct = blockIdx.x, cm0 = 0, cn0 = 0, crow_end = 0;  // cursor: tile, its origin, block
+        int cexp = 0, ckb = 0;
+        auto seek = [&]() {
+            if (ct < num_tiles) {
+                const GroupTile tl = decode_tile<MODE>(ct, p, prefix);
+                cm0 = tl.m0;
+                cn0 = tl.n0;
+                crow_end = tl.row_end;
+                cexp = tl.expert;
+            }
+        };
+        seek();
         auto load_sf = [&]() -> Sf {
             Sf v;
             v.a = 1.0f;
@@ -338,7 +368,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 return v;
             const int kb = ckb;
             const int64_t row = cm0 + quarter * 32 + lane;
-            if (row < p.M)
+            if (row < crow_end)
                 v.a = __ldg(p.sA + (int64_t)kb * p.ld_sA + row);
             if constexpr (MODE == WGRAD) {
 #pragma unroll
@@ -351,16 +381,19 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 #pragma unroll
                 for (int h = 0; h < 2; ++h) {
                     const int64_t nb = cn0 / 128 + h;
-                    if (nb * 128 < p.N)
-                        v.b[h] = MODE == FPROP ? __ldg(p.sB + nb * p.ld_sB + kb)
-                                               : __ldg(p.sB + (int64_t)kb * p.ld_sB + nb);
+                    if (nb * 128 < p.N) {
+                        if constexpr (MODE == GROUPED_C)  // expert block scales [E][N/128][K/128]
+                            v.b[h] = __ldg(p.sB + ((int64_t)cexp * (p.N / 128) + nb) * p.ld_sB + kb);
+                        else
+                            v.b[h] = MODE == FPROP ? __ldg(p.sB + nb * p.ld_sB + kb)
+                                                   : __ldg(p.sB + (int64_t)kb * p.ld_sB + nb);
+                    }
                 }
             }
             if (++ckb == num_kb) {
                 ckb = 0;
                 ct += gridDim.x;
-                if (ct < num_tiles)
-                    decode_tile(ct, p, cm0, cn0);
+                seek();
             }
             return v;
         };
@@ -428,8 +461,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         uint32_t tphase = 0;
         bool ok = true;
         for (int64_t t = blockIdx.x; t < num_tiles && ok; t += gridDim.x) {
-            int64_t m0, n0;
-            decode_tile(t, p, m0, n0);
+            const GroupTile tl = decode_tile<MODE>(t, p, prefix);
+            const int64_t m0 = tl.m0, n0 = tl.n0, row_end = tl.row_end;
             const int64_t col0 = n0 + half * 128;
             const bool cols_ok = col0 < p.N;
             const int64_t rrow0 = m0 + quarter * 32 + (lane >> 2);  // row read back at i = 0
@@ -450,7 +483,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 #pragma unroll
                 for (int i = 0; i < 4; ++i) {
                     const uint4 v = *reinterpret_cast<const uint4 *>(r_ptr + i * 512);
-                    if (rrow0 + 8 * i < p.M)
+                    if (rrow0 + 8 * i < row_end)
                         *reinterpret_cast<uint4 *>(out0 + i * row8 + colb) = v;
                 }
                 __syncwarp();
@@ -596,4 +629,62 @@ extern "C" int fp8_gemm_mx(int mode, const uint8_t *A, const float *sA, int64_t 
     case DGRAD: return launch_out<DGRAD>(out, ta, tb, p, grid, s);
     default: return launch_out<WGRAD>(out, ta, tb, p, grid, s);
     }
+}
+
+extern "C" int fp8_grouped_gemm_mx(const uint8_t *Xq, const float *sX, int64_t ld_sX,
+                                   const int32_t *expert_offsets, int32_t n_experts, int64_t n_rows,
+                                   const uint8_t *Wq, const float *sW, int64_t N, int64_t K, void *Y, int out,
+                                   int64_t ldy, void *stream)
+{
+    if (out != FP8FG_OUT_F32 && out != FP8FG_OUT_BF16)
+        return FP8FG_EINVAL;
+    if (n_rows < 0 || N < 0 || K < BK || N % 128 != 0 || K % BK != 0)
+        return FP8FG_EINVAL;
+    if (n_experts < 1 || n_experts > MAX_EXPERTS)
+        return FP8FG_EINVAL;
+    if (n_rows >= (1ll << 31) || K >= (1ll << 31) || (int64_t)n_experts * N >= (1ll << 31))
+        return FP8FG_EINVAL;
+    const int64_t esz = out == FP8FG_OUT_BF16 ? 2 : 4;
+    if (ld_sX < n_rows || ldy < N || !expert_offsets)
+        return FP8FG_EINVAL;
+    if (n_rows == 0 || N == 0)
+        return FP8FG_OK;
+    if (!Xq || !sX || !Wq || !sW || !Y)
+        return FP8FG_EINVAL;
+    if (!aligned16(Xq) || !aligned16(Wq) || !aligned16(sX) || !aligned16(Y) || K % 16 != 0 || ld_sX % 4 != 0 ||
+        (ldy * esz) % 16 != 0)
+        return FP8FG_EALIGN;
+    if (!device_supported())
+        return FP8FG_EUNSUPPORTED;
+
+    Params p{};
+    p.M = n_rows;
+    p.N = N;
+    p.K = K;
+    p.sA = sX;
+    p.ld_sA = ld_sX;
+    p.sB = sW;
+    p.ld_sB = K / 128;
+    p.C = Y;
+    p.ldc = ldy;
+    p.num_m_tiles = 0;
+    p.num_n_tiles = (N + BN - 1) / BN;
+    p.expert_offsets = expert_offsets;
+    p.n_experts = n_experts;
+    p.n_rows = n_rows;
+    p.status = status_word_ptr();
+    p.wait_limit_ns = wait_limit_ns();
+    p.skip_first_load = take_skip_first_load() ? 1 : 0;
+    if (!p.status)
+        return FP8FG_ECUDA;
+
+    CUtensorMap ta, tb;
+    if (!make_map(&ta, Xq, (uint64_t)K, (uint64_t)n_rows, (uint64_t)K, BK, BM))
+        return FP8FG_ECUDA;
+    if (!make_map(&tb, Wq, (uint64_t)K, (uint64_t)n_experts * (uint64_t)N, (uint64_t)K, BK, BN))
+        return FP8FG_ECUDA;
+    const int grid = sm_count();
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    return out == FP8FG_OUT_BF16 ? launch<GROUPED_C, OUT_BF16>(ta, tb, p, grid > 0 ? grid : 1, s)
+                                 : launch<GROUPED_C, OUT_F32>(ta, tb, p, grid > 0 ? grid : 1, s);
 }

@@ -325,6 +325,24 @@ FP8FG_API int fp8_gemm_mx(int mode,
                          void *C, int out, int64_t ldc, void *stream);
 
 /* ---------------------------------------------------------------------
+ * fp8_grouped_gemm_mx: the MoE expert GEMM of fp8_grouped_gemm (rows
+ * already in expert order, i.e. row_index = NULL) for power-of-two scales,
+ * on the tensor cores' block-scaled MMA as fp8_gemm_mx.
+ *   For each expert e and each row r in [off[e], off[e+1]):
+ *       Y[r][:] = fprop(Xq[r], Wq[e])
+ *   Xq        E4M3 [n_rows][K] (lda = K), e.g. fp8_quant_1x128_gather_pow2.
+ *   sX        FP32 [K/128][ld_sX], ld_sX >= n_rows, powers of two.
+ *   expert_offsets, n_experts, Wq, sW (powers of two), N, K, Y, out, ldy:
+ *             as fp8_grouped_gemm.
+ *   Errors and alignment as fp8_grouped_gemm (malformed offsets are
+ *   reported as FP8FG_EDEVICE through fp8fg_device_status).
+ * ------------------------------------------------------------------- */
+FP8FG_API int fp8_grouped_gemm_mx(const uint8_t *Xq, const float *sX, int64_t ld_sX,
+                         const int32_t *expert_offsets, int32_t n_experts, int64_t n_rows,
+                         const uint8_t *Wq, const float *sW, int64_t N, int64_t K,
+                         void *Y, int out, int64_t ldy, void *stream);
+
+/* ---------------------------------------------------------------------
  * Status and diagnostics (no counterpart on the pages).
  * ------------------------------------------------------------------- */
 
@@ -339,9 +357,10 @@ FP8FG_API int fp8fg_device_status(void *stream);
 /* Library version (major*10000 + minor*100 + patch). */
 FP8FG_API int fp8fg_version(void);
 
-/* Test hook: when `skip` != 0, the next fp8_gemm_blockscaled or fp8_gemm_mx
- * launch on the current device withholds its first operand load (a
- * fp8_grouped_gemm launch clears the request without using it), so the consumers' bounded
+/* Test hook: when `skip` != 0, the next fp8_gemm_blockscaled, fp8_gemm_mx
+ * or fp8_grouped_gemm_mx launch on the current device withholds its first
+ * operand load (a fp8_grouped_gemm launch clears the request without using
+ * it), so the consumers' bounded
  * waits run out and the launch reports FP8FG_ETIMEOUT. One-shot; returns
  * FP8FG_OK. For exercising failure detection without a GPU fault. */
 FP8FG_API int fp8fg_test_skip_first_load(int skip);

@@ -227,3 +227,58 @@ def test_gemm_mx_timeout_is_reported_not_hung():
     wo, swo = oracle.quant_128x128(bits(w), pow2=True)
     c, _, t = oracle.fprop(xo, sxo, wo, swo)
     check_gemm(to_np(y), c, t, False, "mx after timeout")
+
+
+def _moe_small(seed, T=300, K=384, N=256, counts=(0, 1, 129, 0, 300, 5, 128, 0, 257)):
+    g = _gen(seed)
+    x = torch.randn(T, K, generator=g, device=DEV).to(torch.bfloat16)
+    w = (torch.randn(len(counts), N, K, generator=g, device=DEV) * 0.02).to(torch.bfloat16)
+    rng = np.random.default_rng(seed)
+    row_index = np.concatenate([np.sort(rng.choice(T, c, replace=False)) if c else np.zeros(0, np.int64)
+                                for c in counts]).astype(np.int32)
+    off = np.concatenate([[0], np.cumsum(counts)]).astype(np.int32)
+    return x, w, row_index, off
+
+
+@pytest.mark.parametrize("out,counts", [("f32", (0, 1, 129, 0, 300, 5, 128, 0, 257)),
+                                        ("bf16", (40, 64, 2, 65, 17, 33, 32, 0, 1)),
+                                        ("f32", (64, 63, 31, 129, 1))])
+def test_grouped_gemm_mx(out, counts):
+    """MoE experts in the microscaling variant: rows quantised into expert
+    order with power-of-two scales, the grouped GEMM on the block-scaled
+    MMA; expert sizes 0..300 (tiles straddling the next expert's rows);
+    rows past the last offset untouched."""
+    x, w, row_index, off = _moe_small(seed=31, counts=counts)
+    R = int(off[-1])
+    ri = torch.from_numpy(row_index).to(DEV)
+    xg, sxg = fg.fp8_quant_1x128_gather(x, ri, pow2=True)
+    wq, sw = fg.fp8_quant_128x128(w, pow2=True)
+    dt = torch.float32 if out == "f32" else torch.bfloat16
+    y = torch.full((R + 40, w.shape[1]), 5.0, dtype=dt, device=DEV)
+    xg_pad = torch.zeros((R + 40, x.shape[1]), dtype=torch.uint8, device=DEV)
+    xg_pad[:R] = xg
+    sxg_pad = torch.zeros((sxg.shape[0], (R + 40 + 3) // 4 * 4), dtype=torch.float32, device=DEV)
+    sxg_pad[:, :R] = sxg[:, :R]
+    fg.fp8_grouped_gemm_mx(xg_pad, sxg_pad, torch.from_numpy(off).to(DEV), wq, sw, n_rows=R + 40, y=y)
+    assert fg.device_status() == 0
+    assert torch.all(y[R:] == 5.0)
+    xo, sxo = oracle.quant_1x128(bits(x), pow2=True)
+    _same(to_np(xg), xo[row_index], "gathered pow2 codes")
+    wo, swo = to_np(wq), to_np(sw)
+    for e in range(w.shape[0]):
+        qe, se = oracle.quant_128x128(bits(w[e]), pow2=True)
+        _same(wo[e], qe, "expert codes")
+        _same(swo[e], se, "expert scales")
+    c, _, t = oracle.grouped(xo, sxo, row_index, off, wo, swo)
+    check_gemm(to_np(y[:R]), c, t, out == "bf16", "mx grouped")
+
+
+def test_grouped_gemm_mx_bad_offsets_reported():
+    x, w, row_index, off = _moe_small(seed=32, counts=(10, 20))
+    xq, sx = fg.fp8_quant_1x128(x, pow2=True)
+    wq, sw = fg.fp8_quant_128x128(w, pow2=True)
+    bad = torch.tensor([0, 40, 30], dtype=torch.int32, device=DEV)  # decreasing
+    fg.fp8_grouped_gemm_mx(xq, sx, bad, wq, sw, n_rows=300)
+    assert fg.device_status() == 6  # FP8FG_EDEVICE
+    fg.fp8_grouped_gemm_mx(xq, sx, torch.from_numpy(off).to(DEV), wq, sw, n_rows=300)
+    assert fg.device_status() == 0
