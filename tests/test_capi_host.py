@@ -197,3 +197,67 @@ def test_gemm_e4m3_validation(L):
     assert call(ldc=264) == EALIGN
     assert call(M=0) == 0
     assert call() in (EUNSUPPORTED, 4)
+
+
+def test_pow2_quantisers_validate_like_their_counterparts(L):
+    """The power-of-two entry points share the argument checks of the
+    pages' quantisers: the same bad arguments give the same codes."""
+    cases = [dict(), dict(cols=200, ldx=208, ldq=208), dict(lds=2), dict(t=2), dict(x=A8), dict(ldq=264),
+             dict(rows=0), dict(t=1, rows=100)]
+    for kw in cases:
+        a = dict(x=A16, rows=4, cols=256, ldx=256, q=A16, ldq=256, s=A16, lds=4, t=0)
+        a.update(kw)
+        args = (a["x"], a["rows"], a["cols"], a["ldx"], a["q"], a["ldq"], a["s"], a["lds"], a["t"], NULL)
+        assert L.fp8_quant_1x128_pow2(*args) == L.fp8_quant_1x128(*args), kw
+    for kw in [dict(), dict(N=200), dict(K=100), dict(ldw=264), dict(w=A8), dict(N=0)]:
+        a = dict(w=A16, N=256, K=256, ldw=256, q=A16, ldq=256, s=A16)
+        a.update(kw)
+        args = (a["w"], a["N"], a["K"], a["ldw"], a["q"], a["ldq"], a["s"], NULL)
+        assert L.fp8_quant_128x128_pow2(*args) == L.fp8_quant_128x128(*args), kw
+    dual = (A16, 256, 384, 384, A16, 384, A16, 256, A16, 256, A16, 384, NULL)
+    assert L.fp8_quant_1x128_dual_pow2(*dual) == L.fp8_quant_1x128_dual(*dual)
+    bad_dual = (A16, 200, 384, 384, A16, 384, A16, 256, A16, 256, A16, 384, NULL)
+    assert L.fp8_quant_1x128_dual_pow2(*bad_dual) == EINVAL
+    gat = (A16, 64, 256, 256, A16, 8, A16, 256, A16, 8, NULL)
+    assert L.fp8_quant_1x128_gather_pow2(*gat) == L.fp8_quant_1x128_gather(*gat)
+    assert L.fp8_quant_1x128_gather_pow2(A16, 64, 256, 256, NULL, 8, A16, 256, A16, 8, NULL) == EINVAL
+
+
+def test_gemm_mx_validation(L):
+    """fp8_gemm_mx takes fp8_gemm_blockscaled's arguments and checks them the
+    same way."""
+    cases = [dict(mode=3), dict(out=2), dict(K=0), dict(K=200, lda=208, ldb=208), dict(N=200, ldc=208),
+             dict(ldsa=100), dict(ldsb=1), dict(mode=2, ldsb=128), dict(mode=1, ldb=128, ldsb=2), dict(A=A8),
+             dict(lda=264), dict(C=NULL), dict(M=0), dict()]
+    for kw in cases:
+        a = dict(mode=0, A=A16, sA=A16, lda=256, ldsa=128, B=A16, sB=A16, ldb=256, ldsb=2, M=128, N=256, K=256,
+                 C=A16, out=1, ldc=256)
+        a.update(kw)
+        args = (a["mode"], a["A"], a["sA"], a["lda"], a["ldsa"], a["B"], a["sB"], a["ldb"], a["ldsb"], a["M"],
+                a["N"], a["K"], a["C"], a["out"], a["ldc"], NULL)
+        assert L.fp8_gemm_mx(*args) == L.fp8_gemm_blockscaled(*args), kw
+
+
+def test_grouped_gemm_mx_validation(L):
+    f = L.fp8_grouped_gemm_mx
+
+    def call(**kw):
+        a = dict(X=A16, sX=A16, ldsx=100, off=A16, E=4, R=100, W=A16, sW=A16, N=256, K=256, Y=A16, out=1,
+                 ldy=256)
+        a.update(kw)
+        return f(a["X"], a["sX"], a["ldsx"], a["off"], a["E"], a["R"], a["W"], a["sW"], a["N"], a["K"], a["Y"],
+                 a["out"], a["ldy"], NULL)
+
+    assert call(E=0) == EINVAL
+    assert call(E=5000) == EINVAL
+    assert call(K=100) == EINVAL
+    assert call(N=200) == EINVAL
+    assert call(out=2) == EINVAL
+    assert call(ldsx=96) == EINVAL      # ld_sX < n_rows
+    assert call(ldy=128) == EINVAL      # ldy < N
+    assert call(off=NULL) == EINVAL
+    assert call(X=A8) == EALIGN
+    assert call(ldsx=102) == EALIGN
+    assert call(R=0) == 0
+    assert call(Y=NULL) == EINVAL
+    assert call() in (EUNSUPPORTED, 4)
