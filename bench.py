@@ -16,8 +16,8 @@ Other workloads, one JSON line each, for the remaining kernels:
               dY quantised row-wise and transposed (both from one read),
               fprop, dgrad, wgrad
     moe       4096 tokens, 256 experts (2048 x 7168), top-8 with a Zipf(1.1)
-              expert bias: the routed rows of X quantised into expert order
-              (1x128, one pass) + grouped expert GEMM
+              expert bias: X quantised 1x128 once per token and written to
+              its 8 routed rows in expert order + grouped expert GEMM
     outliers  M = 16384 fprop with outlier channels and weight blocks
     tiny      128 x 256 x 128 fprop, FP32 out (latency)
     dense_e4m3  the dense step with the GEMM's output quantised 1x128 in its
@@ -275,7 +275,10 @@ def build(workload, dev, seed, fg, synth):
         T = mo.x.shape[0]
         R = int(mo.expert_offsets[-1].item())
         # the routed rows are quantised straight into expert order (the
-        # dispatch), then each expert's GEMM reads contiguous 128-row tiles
+        # dispatch, in token order: each token read once and written to its
+        # 8 rows), then each expert's GEMM reads contiguous 128-row tiles
+        topk = R // T
+        dest = torch.argsort(mo.row_index.long(), stable=True).to(torch.int32).reshape(T, topk).contiguous()
         xg = torch.empty((R, Kx), dtype=torch.uint8, device=dev)
         sxg = torch.empty((Kx // 128, R), dtype=torch.float32, device=dev)
         y = torch.empty((R, Nw), dtype=torch.bfloat16, device=dev)
@@ -283,8 +286,8 @@ def build(workload, dev, seed, fg, synth):
         moved = nonempty * Nw * Kx + R * Kx + R * Nw * 2 + sw.numel() * 4 + R * (Kx // 128) * 4
         f = 2.0 * R * Nw * Kx
         parts = [
-            Part("quant_x_gather", "quant_rows_kernel<gather>",
-                 lambda: fg.fp8_quant_1x128_gather(mo.x, mo.row_index, q=xg, scales=sxg, pow2=mx), "hbm",
+            Part("quant_x_scatter", "quant_rows_scatter_kernel",
+                 lambda: fg.fp8_quant_1x128_scatter(mo.x, dest, R, q=xg, scales=sxg, pow2=mx), "hbm",
                  2 * T * Kx + (Q1X128_B - 2) * R * Kx + 4 * R),
             Part("grouped", "gemm_mx_kernel<GROUPED_C>" if mx else "gemm_kernel<GROUPED_C>",
                  (lambda: fg.fp8_grouped_gemm_mx(xg, sxg, mo.expert_offsets, wq, sw, R, y=y)) if mx else
@@ -292,7 +295,7 @@ def build(workload, dev, seed, fg, synth):
                  f, extra_bytes=moved),
         ]
         cnt = mo.counts.cpu()
-        W.update(inputs=[mo.x, mo.row_index, mo.expert_offsets], outputs=[y], flops=f,
+        W.update(inputs=[mo.x, dest, mo.expert_offsets], outputs=[y], flops=f,
                  dims={"tokens": T, "experts": E, "N": Nw, "K": Kx, "rows": R, "nonempty_experts": nonempty,
                        "rows_per_expert_max": int(cnt.max()), "rows_per_expert_median": float(cnt.float().median())})
     else:

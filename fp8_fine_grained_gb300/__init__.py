@@ -49,6 +49,8 @@ def lib():
         L.fp8_quant_1x128_gather_pow2.argtypes = L.fp8_quant_1x128_gather.argtypes
         L.fp8_quant_1x128_dual_pow2.argtypes = L.fp8_quant_1x128_dual.argtypes
         L.fp8_quant_128x128_pow2.argtypes = L.fp8_quant_128x128.argtypes
+        L.fp8_quant_1x128_scatter.argtypes = [P, I64, I64, I64, P, I32, I64, P, I64, P, I64, P]
+        L.fp8_quant_1x128_scatter_pow2.argtypes = L.fp8_quant_1x128_scatter.argtypes
         L.fp8_gemm_mx.argtypes = [I32, P, P, I64, I64, P, P, I64, I64, I64, I64, I64, P, I32, I64, P]
         L.fp8_grouped_gemm_mx.argtypes = [P, P, I64, P, ctypes.c_int32, I64, P, P, I64, I64, P, I32, I64, P]
         L.fp8_gemm_blockscaled.argtypes = [I32, P, P, I64, I64, P, P, I64, I64, I64, I64, I64, P, I32, I64, P]
@@ -185,6 +187,32 @@ def fp8_quant_1x128_gather(x, row_index, q=None, scales=None, stream=None, pow2=
     rc = fn(_ptr(x), n_src, cols, x.stride(0), _ptr(row_index), rows, _ptr(q),
             q.stride(0), _ptr(scales), scales.stride(0), _stream(stream))
     _check(rc, "fp8_quant_1x128_gather_pow2" if pow2 else "fp8_quant_1x128_gather")
+    return q, scales
+
+
+def fp8_quant_1x128_scatter(x, dest_index, n_out, q=None, scales=None, stream=None, pow2=False):
+    """1x128 quantisation of every row of x, written to its k destination
+    rows dest_index[r, :] (int32 [n_src, k]; negative = not written):
+    q uint8 [n_out, cols], scales float32 [cols/128, ld_s>=n_out]. Equal to
+    fp8_quant_1x128_gather with the inverse index; each row is read once."""
+    torch = _torch()
+    _rowmajor(x, "x")
+    if x.dtype != torch.bfloat16:
+        raise ValueError("x must be bfloat16")
+    if dest_index.dtype != torch.int32 or not dest_index.is_contiguous() or dest_index.dim() != 2:
+        raise ValueError("dest_index must be contiguous int32 [n_src, k]")
+    n_src, cols = x.shape
+    if dest_index.shape[0] != n_src:
+        raise ValueError("dest_index needs one row per source row")
+    k = dest_index.shape[1]
+    if q is None:
+        q = torch.empty((n_out, cols), dtype=torch.uint8, device=x.device)
+    if scales is None:
+        scales = torch.empty((cols // 128, _pad(max(n_out, 1), 4)), dtype=torch.float32, device=x.device)
+    fn = lib().fp8_quant_1x128_scatter_pow2 if pow2 else lib().fp8_quant_1x128_scatter
+    rc = fn(_ptr(x), n_src, cols, x.stride(0), _ptr(dest_index), k, n_out, _ptr(q), q.stride(0), _ptr(scales),
+            scales.stride(0), _stream(stream))
+    _check(rc, "fp8_quant_1x128_scatter_pow2" if pow2 else "fp8_quant_1x128_scatter")
     return q, scales
 
 

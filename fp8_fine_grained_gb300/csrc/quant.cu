@@ -1,5 +1,5 @@
 // Fine-grained E4M3 quantisation kernels: 1x128 tiles (per row, also for
-// rows gathered through a row index), 128x1 tiles with transposed output
+// rows gathered through a row index or scattered to several destinations), 128x1 tiles with transposed output
 // (per column, for the weight-gradient operands), both of those from one
 // read, and 128x128 blocks (weights).
 //
@@ -149,6 +149,83 @@ __global__ void __launch_bounds__(256, 8) quant_rows_kernel(const uint16_t *__re
         const int64_t row = r0 + rr, gs = gb * QR_GROUPS + gg;
         if (row < rows && gs < ngroups)
             scales[gs * ld_s + row] = s_scale[gg][rr];
+    }
+}
+
+// ------------------------------------- 1x128 per row, scattered copies ----
+// The MoE dispatch in token order: every source row is read and quantised
+// once (the tile and group rule of quant_rows_kernel) and its codes and
+// scales are written to each of its k destination rows dest_index[r*k + j]
+// (rows grouped by expert). A negative destination is not written; one at or
+// beyond n_out is reported as FP8FG_EDEVICE and not written. The output
+// equals gathering rows of the plain 1x128 quantisation.
+constexpr int SCATTER_MAX_K = 16;
+
+template <bool P2>
+__global__ void __launch_bounds__(256, 8) quant_rows_scatter_kernel(const uint16_t *__restrict__ x, int64_t rows,
+                                                                    int64_t ngroups, int64_t ldx,
+                                                                    uint8_t *__restrict__ q, int64_t ldq,
+                                                                    float *__restrict__ scales, int64_t ld_s,
+                                                                    int64_t tiles_g, const int32_t *__restrict__ dest,
+                                                                    int k, int64_t n_out, int *status)
+{
+    __shared__ float s_scale[QR_GROUPS][QR_ROWS];
+    __shared__ int32_t s_dst[QR_ROWS][SCATTER_MAX_K];
+    const int hw = threadIdx.x >> 4;
+    const int l = threadIdx.x & 15;
+    const int64_t gb = blockIdx.x % tiles_g, rb = blockIdx.x / tiles_g;
+    const int64_t r0 = rb * QR_ROWS;
+    const int64_t g = gb * QR_GROUPS + hw;
+    const bool g_ok = g < ngroups;
+    if (threadIdx.x < QR_ROWS * k) {
+        const int rr = threadIdx.x / k, j = threadIdx.x % k;
+        int32_t d = -1;
+        if (r0 + rr < rows) {
+            d = dest[(r0 + rr) * k + j];
+            if (d >= n_out) {
+                atomicCAS(status, 0, FP8FG_EDEVICE);
+                d = -1;
+            }
+        }
+        s_dst[rr][j] = d;
+    }
+    const uint16_t *src = x + r0 * ldx + g * GROUP + l * 8;
+    uint4 v[QR_ITEMS];
+#pragma unroll
+    for (int i = 0; i < QR_ITEMS; ++i)
+        v[i] = (g_ok && r0 + i < rows) ? ld_stream_v4(src + (int64_t)i * ldx) : make_uint4(0, 0, 0, 0);
+    uint32_t m[QR_ITEMS];
+#pragma unroll
+    for (int i = 0; i < QR_ITEMS; ++i) {
+        m[i] = absmax_bits8(v[i]);
+#pragma unroll
+        for (int off = 8; off >= 1; off >>= 1)
+            m[i] = max(m[i], __shfl_xor_sync(0xffffffffu, m[i], off));
+    }
+    float sc[QR_ITEMS], inv[QR_ITEMS];
+    group_scales_batched<QR_ITEMS, P2>(m, sc, inv);
+    __syncthreads();  // destinations
+#pragma unroll
+    for (int i = 0; i < QR_ITEMS; ++i) {
+        if (g_ok && r0 + i < rows) {
+            const uint2 code = quant8(v[i], inv[i]);
+            for (int j = 0; j < k; ++j) {
+                const int32_t d = s_dst[i][j];
+                if (d >= 0)
+                    *reinterpret_cast<uint2 *>(q + (int64_t)d * ldq + g * GROUP + l * 8) = code;
+            }
+            if (l == 0)
+                s_scale[hw][i] = sc[i];
+        }
+    }
+    __syncthreads();
+    for (int idx = threadIdx.x; idx < QR_GROUPS * QR_ROWS * k; idx += blockDim.x) {
+        const int gg = idx / (QR_ROWS * k), rem = idx % (QR_ROWS * k);
+        const int rr = rem / k, j = rem % k;
+        const int64_t gs = gb * QR_GROUPS + gg;
+        const int32_t d = s_dst[rr][j];
+        if (r0 + rr < rows && gs < ngroups && d >= 0)
+            scales[gs * ld_s + d] = s_scale[gg][rr];
     }
 }
 
@@ -415,6 +492,35 @@ int quant_1x128_gather(const void *x, int64_t n_src, int64_t cols, int64_t ldx,
 }
 
 template <bool P2>
+int quant_1x128_scatter(const void *x, int64_t n_src, int64_t cols, int64_t ldx, const int32_t *dest_index, int k,
+                        int64_t n_out, uint8_t *q, int64_t ldq, float *scales, int64_t ld_s, void *stream)
+{
+    if (n_src < 0 || n_out < 0 || cols < 0 || cols % GROUP != 0 || k < 1 || k > SCATTER_MAX_K || ldx < cols ||
+        ldq < cols || ld_s < n_out)
+        return FP8FG_EINVAL;
+    if (n_src == 0 || n_out == 0 || cols == 0)
+        return FP8FG_OK;
+    if (!x || !dest_index || !q || !scales)
+        return FP8FG_EINVAL;
+    if (!aligned16(x) || !aligned16(q) || !aligned16(scales) || ldx % 8 != 0 || ldq % 16 != 0 || ld_s % 4 != 0)
+        return FP8FG_EALIGN;
+    if (!device_supported())
+        return FP8FG_EUNSUPPORTED;
+    int *status = status_word_ptr();
+    if (!status)
+        return FP8FG_ECUDA;
+    const int64_t ngroups = cols / GROUP;
+    const int64_t tiles_g = (ngroups + QR_GROUPS - 1) / QR_GROUPS;
+    const int64_t tiles = tiles_g * ((n_src + QR_ROWS - 1) / QR_ROWS);
+    if (tiles > 0x7FFFFFFF)
+        return FP8FG_EINVAL;
+    quant_rows_scatter_kernel<P2><<<(unsigned)tiles, 256, 0, static_cast<cudaStream_t>(stream)>>>(
+        static_cast<const uint16_t *>(x), n_src, ngroups, ldx, q, ldq, scales, ld_s, tiles_g, dest_index, k, n_out,
+        status);
+    return launch_status();
+}
+
+template <bool P2>
 int quant_1x128_dual(const void *x, int64_t rows, int64_t cols, int64_t ldx, uint8_t *q,
                                     int64_t ldq, float *scales, int64_t ld_s, uint8_t *qT, int64_t ldqT,
                                     float *scalesT, int64_t ld_sT, void *stream)
@@ -478,6 +584,20 @@ extern "C" int fp8_quant_1x128_gather(const void *x, int64_t n_src, int64_t cols
                                       int64_t ld_s, void *stream)
 {
     return quant_1x128_gather<false>(x, n_src, cols, ldx, row_index, rows, q, ldq, scales, ld_s, stream);
+}
+
+extern "C" int fp8_quant_1x128_scatter(const void *x, int64_t n_src, int64_t cols, int64_t ldx,
+                                       const int32_t *dest_index, int k, int64_t n_out, uint8_t *q, int64_t ldq,
+                                       float *scales, int64_t ld_s, void *stream)
+{
+    return quant_1x128_scatter<false>(x, n_src, cols, ldx, dest_index, k, n_out, q, ldq, scales, ld_s, stream);
+}
+
+extern "C" int fp8_quant_1x128_scatter_pow2(const void *x, int64_t n_src, int64_t cols, int64_t ldx,
+                                            const int32_t *dest_index, int k, int64_t n_out, uint8_t *q,
+                                            int64_t ldq, float *scales, int64_t ld_s, void *stream)
+{
+    return quant_1x128_scatter<true>(x, n_src, cols, ldx, dest_index, k, n_out, q, ldq, scales, ld_s, stream);
 }
 
 extern "C" int fp8_quant_1x128_dual(const void *x, int64_t rows, int64_t cols, int64_t ldx, uint8_t *q,

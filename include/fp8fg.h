@@ -157,6 +157,31 @@ FP8FG_API int fp8_quant_1x128_gather(const void *x, int64_t n_src, int64_t cols,
                            void *stream);
 
 /* ---------------------------------------------------------------------
+ * fp8_quant_1x128_scatter: the same dispatch in token order.
+ * Source: as fp8_quant_1x128_gather (yunhecapital.com 2.2.3: FP8 for the
+ * dispatch; 2.2.2 and tonho.wtf "como funciona": 8 of 256 routed experts
+ * per token).
+ *
+ * Every source row r of x is read and quantised once (1x128 rule) and
+ * written to its k destination rows d = dest_index[r*k + j], j < k:
+ * q[d][:] and scales[g*ld_s + d]. The result equals
+ * fp8_quant_1x128_gather with the inverse index, while each token is read
+ * once instead of once per copy.
+ *   x           bf16 [n_src][ldx]; cols % 128 == 0.
+ *   dest_index  int32 [n_src][k], device; 1 <= k <= 16. A negative entry
+ *               is not written; an entry >= n_out is reported as
+ *               FP8FG_EDEVICE through fp8fg_device_status and not written.
+ *   q           E4M3 [n_out][ldq]; scales FP32 [cols/128][ld_s],
+ *               ld_s >= n_out. Rows no entry points to are left untouched.
+ *   Alignment as fp8_quant_1x128. fp8_quant_1x128_scatter_pow2 is the
+ *   power-of-two variant (see below).
+ * ------------------------------------------------------------------- */
+FP8FG_API int fp8_quant_1x128_scatter(const void *x, int64_t n_src, int64_t cols, int64_t ldx,
+                           const int32_t *dest_index, int k, int64_t n_out,
+                           uint8_t *q, int64_t ldq, float *scales, int64_t ld_s,
+                           void *stream);
+
+/* ---------------------------------------------------------------------
  * fp8_quant_128x128: weight quantisation in 128x128 blocks.
  * Source: innerforce.co.kr, fine-grained quantization paragraph ("per 128
  * input channels per 128 output channels"); yunhecapital.com 2.2.3;
@@ -286,9 +311,11 @@ FP8FG_API int fp8_grouped_gemm(const uint8_t *Xq, const float *sX, int64_t ld_sX
  * as the entry points above, so either GEMM accepts them.
  *
  * fp8_quant_1x128_pow2, fp8_quant_1x128_dual_pow2,
- * fp8_quant_1x128_gather_pow2, fp8_quant_128x128_pow2: arguments, layouts,
- * alignment and errors exactly as fp8_quant_1x128, fp8_quant_1x128_dual,
- * fp8_quant_1x128_gather and fp8_quant_128x128; only the scale rule differs.
+ * fp8_quant_1x128_gather_pow2, fp8_quant_1x128_scatter_pow2,
+ * fp8_quant_128x128_pow2: arguments, layouts, alignment and errors exactly
+ * as fp8_quant_1x128, fp8_quant_1x128_dual, fp8_quant_1x128_gather,
+ * fp8_quant_1x128_scatter and fp8_quant_128x128; only the scale rule
+ * differs.
  * ------------------------------------------------------------------- */
 FP8FG_API int fp8_quant_1x128_pow2(const void *x, int64_t rows, int64_t cols, int64_t ldx,
                          uint8_t *q, int64_t ldq, float *scales, int64_t ld_s,
@@ -299,6 +326,9 @@ FP8FG_API int fp8_quant_1x128_dual_pow2(const void *x, int64_t rows, int64_t col
                          void *stream);
 FP8FG_API int fp8_quant_1x128_gather_pow2(const void *x, int64_t n_src, int64_t cols, int64_t ldx,
                          const int32_t *row_index, int64_t rows,
+                         uint8_t *q, int64_t ldq, float *scales, int64_t ld_s, void *stream);
+FP8FG_API int fp8_quant_1x128_scatter_pow2(const void *x, int64_t n_src, int64_t cols, int64_t ldx,
+                         const int32_t *dest_index, int k, int64_t n_out,
                          uint8_t *q, int64_t ldq, float *scales, int64_t ld_s, void *stream);
 FP8FG_API int fp8_quant_128x128_pow2(const void *w, int64_t N, int64_t K, int64_t ldw,
                          uint8_t *q, int64_t ldq, float *scales, void *stream);

@@ -261,3 +261,26 @@ def test_grouped_gemm_mx_validation(L):
     assert call(R=0) == 0
     assert call(Y=NULL) == EINVAL
     assert call() in (EUNSUPPORTED, 4)
+
+
+def test_quant_scatter_validation(L):
+    f = L.fp8_quant_1x128_scatter
+
+    def call(**kw):
+        a = dict(x=A16, n=64, cols=256, ldx=256, d=A16, k=8, n_out=512, q=A16, ldq=256, s=A16, lds=512)
+        a.update(kw)
+        return f(a["x"], a["n"], a["cols"], a["ldx"], a["d"], a["k"], a["n_out"], a["q"], a["ldq"], a["s"],
+                 a["lds"], NULL)
+
+    assert call(k=0) == EINVAL
+    assert call(k=17) == EINVAL
+    assert call(cols=200, ldx=208, ldq=208) == EINVAL
+    assert call(lds=500) == EINVAL      # ld_s < n_out
+    assert call(d=NULL) == EINVAL
+    assert call(x=A8) == EALIGN
+    assert call(lds=514) == EALIGN
+    assert call(n=0) == 0
+    assert call(n_out=0, lds=0) == 0
+    assert call() in (EUNSUPPORTED, 4)
+    args = (A16, 64, 256, 256, A16, 8, 512, A16, 256, A16, 500, NULL)
+    assert L.fp8_quant_1x128_scatter_pow2(*args) == f(*args) == EINVAL

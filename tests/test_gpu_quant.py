@@ -158,6 +158,52 @@ def test_quant_1x128_gather_bad_index_reported():
     assert np.array_equal(to_np(q), qo)
 
 
+def _routing(n_src, k, seed):
+    """Destinations of k copies of every source row, grouped by expert the
+    way top-k routing makes them: a random permutation of n_src*k rows."""
+    perm = np.random.default_rng(seed).permutation(n_src * k).astype(np.int32)
+    return perm.reshape(n_src, k)
+
+
+@pytest.mark.parametrize("n_src,k,cols", [(1, 1, 128), (37, 8, 384), (300, 3, 7168), (4096, 8, 1024)])
+@pytest.mark.parametrize("pow2", [False, True])
+def test_quant_1x128_scatter(n_src, k, cols, pow2):
+    """Every source row quantised once and written to its k destination rows
+    equals the oracle's 1x128 quantisation of the gathered rows."""
+    x = _x(n_src, cols, seed=n_src + k + cols)
+    dest = _routing(n_src, k, seed=n_src * k)
+    n_out = n_src * k
+    q, s = fg.fp8_quant_1x128_scatter(x, torch.from_numpy(dest).to(DEV), n_out, pow2=pow2)
+    assert fg.device_status() == 0
+    src_of = np.empty(n_out, np.int64)
+    src_of[dest.reshape(-1)] = np.repeat(np.arange(n_src), k)
+    qo, so = oracle.quant_1x128(bits(x)[src_of], pow2=pow2)
+    assert np.array_equal(to_np(q), qo)
+    assert np.array_equal(rows_scales(s, n_out).view(np.uint32), so.view(np.uint32))
+
+
+def test_quant_1x128_scatter_skips_and_reports():
+    """Negative destinations are not written and leave their rows untouched;
+    a destination past the output is reported and not written."""
+    x = _x(8, 256, seed=7)
+    dest = np.array([[0, -1], [3, 1], [-1, -1], [2, 50], [4, 5], [6, 7], [8, 9], [10, 11]], np.int32)
+    n_out = 12
+    q = torch.full((n_out, 256), 0xAB, dtype=torch.uint8, device=DEV)
+    s = torch.full((2, 12), -1.0, dtype=torch.float32, device=DEV)
+    fg.fp8_quant_1x128_scatter(x, torch.from_numpy(dest).to(DEV), n_out, q=q, scales=s)
+    assert fg.device_status() == 6  # FP8FG_EDEVICE for the 50
+    qo, so = oracle.quant_1x128(bits(x))
+    qg, sg = to_np(q), to_np(s)
+    for r in range(8):
+        for d in dest[r]:
+            if 0 <= d < n_out:
+                assert np.array_equal(qg[d], qo[r])
+                assert np.array_equal(sg[:, d], so[r])
+    untouched = sorted(set(range(n_out)) - {int(d) for d in dest.reshape(-1) if 0 <= d < n_out})
+    for d in untouched:
+        assert np.all(qg[d] == 0xAB) and np.all(sg[:, d] == -1.0)
+
+
 def test_quant_zero_size_is_noop():
     x = torch.empty(0, 256, dtype=torch.bfloat16, device=DEV)
     q, s = fg.fp8_quant_1x128(x)
