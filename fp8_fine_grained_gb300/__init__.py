@@ -367,12 +367,18 @@ def fp8_grouped_gemm_mx(xq, sx, expert_offsets, wq, sw, n_rows, out_dtype=None, 
     """fp8_grouped_gemm with rows already in expert order (row_index=None)
     for power-of-two scales, on the tensor cores' block-scaled MMA."""
     torch = _torch()
-    for t, n in ((xq, "xq"), (sx, "sx"), (wq, "wq"), (sw, "sw")):
-        if not t.is_contiguous() and n != "sx":
-            raise ValueError(n + " must be contiguous")
+    _rowmajor(xq, "xq")
+    _rowmajor(sx, "sx")
+    if not (wq.is_contiguous() and sw.is_contiguous()):
+        raise ValueError("wq and sw must be contiguous")
     if expert_offsets.dtype != torch.int32 or not expert_offsets.is_contiguous():
         raise ValueError("expert_offsets must be contiguous int32")
     E, N, K = wq.shape
+    T, K2 = xq.shape
+    if K2 != K or xq.stride(0) != K:
+        raise ValueError("xq must be [n_rows, K] contiguous with the experts' K")
+    if T < n_rows or sx.shape[1] < n_rows:
+        raise ValueError("xq and sx must hold n_rows rows")
     if out_dtype is None:
         out_dtype = torch.bfloat16
     if y is None:
