@@ -11,7 +11,9 @@
 // and per column of B for each 32-wide contraction step and applies them
 // inside the MMA, so the whole contraction accumulates in tensor memory and
 // no partial sum leaves the tensor cores until the epilogue. A 128-wide
-// group's scale is written once per block and read by its four K steps.
+// group's scale is one byte in TMEM that all four of its K steps read.
+// Modes: fprop, dgrad, wgrad, and MoE experts over rows already in expert
+// order (the tiles of group_tiles.cuh).
 //
 // GB300 design (one CTA per SM, persistent over 128x256 output tiles, 16
 // warps):
