@@ -553,14 +553,29 @@ def cpu_sample(workload, rows, seed=0):
     return dt, 2.0 * rows * N * K, oracle.num_threads()
 
 
-def cpu_baseline(workload, budget_s=15.0):
+def cpu_baseline(workload, budget_s=15.0, single_s=None):
+    """The oracle on a bounded sample of the workload, on all host cores,
+    and (``single_thread``) on one core over a smaller sample."""
+    import oracle
+
     M, K, N = oracle_dims(workload)
     dt, fl, th = cpu_sample(workload, 8)
     rows = max(8, min(M, int(8 * budget_s / max(dt, 1e-3))))
     dt, fl, th = cpu_sample(workload, rows)
-    return {"value": round(fl / dt / 1e12, 6), "unit": "TFLOP/s", "cores": th, "kind": "oracle",
-            "sample": "%d of %d rows of X quantised 1x128 and multiplied by the full %dx%d W "
-                      "(W quantised outside the timing); %.1f s" % (rows, M, N, K, dt)}
+    out = {"value": round(fl / dt / 1e12, 6), "unit": "TFLOP/s", "cores": th, "kind": "oracle",
+           "sample": "%d of %d rows of X quantised 1x128 and multiplied by the full %dx%d W "
+                     "(W quantised outside the timing); %.1f s" % (rows, M, N, K, dt)}
+    single_s = budget_s / 3 if single_s is None else single_s
+    per_row = dt / rows * th  # one core, if the oracle scales with its threads
+    rows1 = max(1, min(M, int(single_s / max(per_row, 1e-6))))
+    oracle.set_num_threads(1)
+    try:
+        dt1, fl1, th1 = cpu_sample(workload, rows1)
+    finally:
+        oracle.set_num_threads(th)
+    out["single_thread"] = {"value": round(fl1 / dt1 / 1e12, 6), "cores": th1,
+                            "sample": "%d rows; %.1f s" % (rows1, dt1)}
+    return out
 
 
 def run_reference(args):

@@ -52,6 +52,7 @@ def lib():
         L.orc_gemm_blockscaled.argtypes = [P, P, P, P, I64, I64, I64, P, I64, P, P, P]
         L.orc_f32_to_bf16.argtypes = [P, I64, P]
         L.orc_num_threads.restype = ctypes.c_int
+        L.orc_set_num_threads.argtypes = [ctypes.c_int]
         _lib = L
     return _lib
 
@@ -247,6 +248,11 @@ def grouped(xq, sx, row_index, expert_offsets, wq, sw, rows=None, want_exact=Tru
 def num_threads():
     """Threads the oracle's OpenMP regions run on."""
     return int(lib().orc_num_threads())
+
+
+def set_num_threads(n):
+    """Run the oracle's OpenMP regions on n threads from now on."""
+    lib().orc_set_num_threads(int(n))
 
 
 def to_bf16_bits(c):

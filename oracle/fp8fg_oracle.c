@@ -368,6 +368,14 @@ void orc_f32_to_bf16(const float *v, int64_t n, uint16_t *out)
 
 int orc_version(void) { return 1; }
 
+/* Threads the following OpenMP regions of this library use (n >= 1); for
+ * timing the oracle on one core against all of them. */
+void orc_set_num_threads(int n)
+{
+    if (n >= 1)
+        omp_set_num_threads(n);
+}
+
 /* Threads an OpenMP parallel region of this library uses. */
 int orc_num_threads(void)
 {

@@ -74,3 +74,13 @@ def test_reduce_max_over_two_gloo_ranks():
 
 def test_reduce_max_single_process_is_identity():
     assert bench.reduce_max([3.0, 1.0], None) == [3.0, 1.0]
+
+
+def test_cpu_baseline_reports_all_cores_and_one_core():
+    cb = bench.cpu_baseline("tiny", budget_s=0.3, single_s=0.1)
+    assert cb["kind"] == "oracle" and cb["unit"] == "TFLOP/s"
+    assert cb["value"] > 0 and cb["cores"] >= 1
+    st = cb["single_thread"]
+    assert st["cores"] == 1 and st["value"] > 0
+    import oracle
+    assert oracle.num_threads() == cb["cores"]  # restored afterwards
