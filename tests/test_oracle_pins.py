@@ -538,3 +538,29 @@ def test_page_constants_fixture():
     assert consts["weight_block_rows"] == consts["weight_block_cols"] == oracle.GROUP
     assert consts["promotion_interval"] == oracle.GROUP
     assert consts["e4m3_max"] == oracle.E4M3_MAX == float(np.nanmax(oracle.e4m3_decode_table()))
+
+
+def test_results_do_not_depend_on_the_thread_count():
+    # the oracle's OpenMP loops split rows and output elements only, so one
+    # thread and all threads must give the same bytes, scales and sums
+    rng = np.random.default_rng(21)
+    x = (rng.standard_normal((256, 512)) * np.exp(rng.standard_normal(512))).astype(np.float32)
+    w = (rng.standard_normal((384, 512)) * 0.02).astype(np.float32)
+    xb, wb = bf16_bits_of(x), bf16_bits_of(w)
+    n = oracle.num_threads()
+
+    def run():
+        xq, sx = oracle.quant_1x128(xb)
+        xt, st = oracle.quant_128x1_t(xb)
+        wq, sw = oracle.quant_128x128(wb)
+        c, ce, t = oracle.fprop(xq, sx, wq, sw)
+        return [xq, sx, xt, st, wq, sw, c, ce, t]
+
+    many = run()
+    oracle.set_num_threads(1)
+    try:
+        one = run()
+    finally:
+        oracle.set_num_threads(n)
+    for a, b in zip(many, one):
+        assert a.dtype == b.dtype and np.array_equal(a.view(np.uint8), b.view(np.uint8))
