@@ -45,6 +45,7 @@ import os
 import statistics
 import subprocess
 import sys
+import tempfile
 import time
 
 ROOT = os.path.dirname(os.path.abspath(__file__))
@@ -105,22 +106,32 @@ def reduce_max(values, pg):
 
 
 class ClockSampler:
-    """nvidia-smi clock/throttle sampling during the timed region."""
+    """nvidia-smi clock/throttle sampling (every 50 ms, each sample with its
+    timestamp) around the timed region; the summary keeps only the samples
+    taken inside it."""
 
-    def __init__(self, index, out_path):
+    FIELDS = ("timestamp,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index, out_path=None):
         self.index = index
+        if out_path is None:
+            fd, out_path = tempfile.mkstemp(prefix="fp8fg_clocks_", suffix=".csv")
+            os.close(fd)
+            self.tmp = True
+        else:
+            self.tmp = False
         self.out_path = out_path
         self.proc = None
         self.f = None
+        self.regions = []
 
     def __enter__(self):
         try:
             self.f = open(self.out_path, "w")
             self.proc = subprocess.Popen(
-                ["nvidia-smi", "-i", str(self.index),
-                 "--query-gpu=clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
-                 "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
-                 "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap",
+                ["nvidia-smi", "-i", str(self.index), "--query-gpu=" + self.FIELDS,
                  "--format=csv,noheader,nounits", "-lms", "50"],
                 stdout=self.f, stderr=subprocess.DEVNULL)
         except OSError:
@@ -128,8 +139,13 @@ class ClockSampler:
         time.sleep(0.3)
         return self
 
+    def mark(self, t0, t1):
+        """Host wall-clock bounds of one timed region."""
+        self.regions.append((t0, t1))
+
     def __exit__(self, *a):
         if self.proc is not None:
+            time.sleep(0.1)
             self.proc.terminate()
             try:
                 self.proc.wait(timeout=5)
@@ -138,32 +154,73 @@ class ClockSampler:
         if self.f is not None:
             self.f.close()
 
-    def summary(self):
-        return summarize_clocks(self.out_path)
+    def summary(self, region=None):
+        out = summarize_clocks(self.out_path, [region] if region else self.regions)
+        return out
+
+    def cleanup(self):
+        if self.tmp:
+            try:
+                os.unlink(self.out_path)
+            except OSError:
+                pass
 
 
-def summarize_clocks(path):
-    sm, mx, reasons = [], 0.0, set()
+def _stamp(text):
+    """nvidia-smi timestamp (local time) -> seconds since the epoch."""
+    import datetime
+    for fmt in ("%Y/%m/%d %H:%M:%S.%f", "%Y/%m/%d %H:%M:%S"):
+        try:
+            return datetime.datetime.strptime(text.strip(), fmt).timestamp()
+        except ValueError:
+            continue
+    return None
+
+
+def summarize_clocks(path, regions):
+    """Median SM clock, the maximum and every throttle reason seen, over the
+    samples whose timestamp falls inside one of the timed regions. With no
+    sample inside (a region shorter than the 50 ms sampling interval), the
+    clock is reported as None and the nearest samples (within 0.25 s of a
+    region) are summarised separately, labelled as such."""
     names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+    rows = []
     try:
         for line in open(path):
-            parts = [p.strip() for p in line.split(",")]
-            if len(parts) < 8:
+            parts = [q.strip() for q in line.split(",")]
+            if len(parts) < 9:
                 continue
+            ts = _stamp(parts[0])
             try:
-                sm.append(float(parts[0]))
-                mx = max(mx, float(parts[1]))
+                sm, mx = float(parts[1]), float(parts[2])
             except ValueError:
                 continue
-            for n, v in zip(names, parts[4:8]):
-                if v.lower() == "active":
-                    reasons.add(n)
+            rows.append((ts, sm, mx, {n for n, v in zip(names, parts[5:9]) if v.lower() == "active"}))
     except OSError:
         pass
-    if not sm:
+
+    def pick(slack):
+        return [r for r in rows if r[0] is not None and any(a - slack <= r[0] <= b + slack for a, b in regions)]
+
+    def summ(sel):
+        return {"sm_mhz": statistics.median(r[1] for r in sel), "sm_max_mhz": max(r[2] for r in sel),
+                "reasons": sorted(set().union(*(r[3] for r in sel))), "samples": len(sel)}
+
+    if not rows:
         return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"], "samples": 0}
-    loaded = [v for v in sm if v > 0.5 * mx] or sm
-    return {"sm_mhz": statistics.median(loaded), "sm_max_mhz": mx, "reasons": sorted(reasons), "samples": len(sm)}
+    inside = pick(0.0)
+    timed_s = round(sum(b - a for a, b in regions), 4)
+    if inside:
+        out = summ(inside)
+        out["timed_region_s"] = timed_s
+        return out
+    near = pick(0.25)
+    out = {"sm_mhz": None, "sm_max_mhz": max(r[2] for r in rows), "reasons": [], "samples": 0,
+           "timed_region_s": timed_s,
+           "note": "no nvidia-smi sample (50 ms interval) fell inside the timed region"}
+    if near:
+        out["within_0.25s_of_timed_region"] = summ(near)
+    return out
 
 
 # --------------------------------------------------------------- workloads ----
@@ -327,137 +384,50 @@ def load_traffic(workload):
     return d.get(workload, {})
 
 
-def run_ours(args):
+def time_parts(W, args, pg, clocks, stream, flush_l2):
+    """W untimed warm-up steps, then exactly K timed steps of the workload's
+    parts, each part between CUDA events on the launching stream, L2 flushed
+    before every step outside the events. Returns the mean ms of every part
+    (max over ranks) and the host bounds of the timed region."""
     import torch
 
     import fp8_fine_grained_gb300 as fg
-    from fp8_fine_grained_gb300 import synth
-
-    world, rank, local = dist_env()
-    torch.cuda.set_device(local)
-    dev = torch.device("cuda", local)
-    pg = None
-    if world > 1:
-        import torch.distributed as dist
-        dist.init_process_group("nccl")
-        pg = dist
-
-    W = build(args.workload, dev, rank, fg, synth)
     parts = W["parts"]
-    flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
-    clean = torch.ones(L2_CLEAN_BYTES // 4, dtype=torch.float32, device=dev)
-    sink = torch.empty((), dtype=torch.float32, device=dev)
-    stream = torch.cuda.current_stream()
-
-    def flush_l2():
-        flush.zero_()
-        torch.sum(clean, dim=0, out=sink)
-
+    n = len(parts)
+    # warm-up right before the timed loop (after the clock sampler started),
+    # so that clocks and memory are at their working state when timing starts
     for _ in range(args.warmup):
+        flush_l2()
         for p_ in parts:
             p_.fn()
     torch.cuda.synchronize()
     if fg.device_status() != 0:
         raise RuntimeError("device status after warm-up")
-
-    n = len(parts)
     ev = [[torch.cuda.Event(enable_timing=True) for _ in range(n + 1)] for _ in range(args.steps)]
-    hbm, bf16, peak_kind = peaks()
-    fp8_peak = 2.0 * bf16   # nominal FP8/BF16 dense ratio 4.5/2.25 on the measured BF16 burst
-    clk_path = os.path.join(ROOT, "gpurun_out", "bench_clocks_rank%d.csv" % rank) \
-        if os.path.isdir(os.path.join(ROOT, "gpurun_out")) else "/tmp/fp8fg_clocks_%d.csv" % rank
-    clocks = ClockSampler(local, clk_path)
     if pg:
         pg.barrier()
     torch.cuda.synchronize()
-    with clocks:
-        for i in range(args.steps):
-            flush_l2()                           # outside the events
-            ev[i][0].record(stream)
-            for j, p_ in enumerate(parts):
-                p_.fn()
-                ev[i][j + 1].record(stream)
-        torch.cuda.synchronize()
+    t0 = time.time()
+    for i in range(args.steps):
+        flush_l2()                           # outside the events
+        ev[i][0].record(stream)
+        for j, p_ in enumerate(parts):
+            p_.fn()
+            ev[i][j + 1].record(stream)
+    torch.cuda.synchronize()
+    t1 = time.time()
+    clocks.mark(t0, t1)
     if pg:
         pg.barrier()
     if fg.device_status() != 0:
         raise RuntimeError("device status after timing")
     part_ms = [sum(ev[i][j].elapsed_time(ev[i][j + 1]) for i in range(args.steps)) / args.steps
                for j in range(n)]
+    return reduce_max(part_ms, pg), (t0, t1)
 
-    # end to end through the public API: every step uploads its inputs from
-    # pinned host memory, runs the step and reads its outputs back into
-    # pinned host memory. Two copies of the workload's device buffers and
-    # three streams let step i's upload, step i-1's kernels and step i-2's
-    # read-back run at the same time (as a data loader feeding a training
-    # or serving loop does); each step still moves all of its bytes.
-    e2e = None
-    if args.workload in WORKLOADS:
-        sets = [W, build(args.workload, dev, rank, fg, synth)]
-        hin = [t.cpu().pin_memory() for t in W["inputs"]]
-        hout = [[torch.empty(t.shape, dtype=t.dtype).pin_memory() for t in S["outputs"]] for S in sets]
-        s_in, s_cmp, s_out = torch.cuda.Stream(), torch.cuda.Stream(), torch.cuda.Stream()
-        in_done = [torch.cuda.Event() for _ in sets]
-        cmp_done = [torch.cuda.Event() for _ in sets]
-        out_done = [torch.cuda.Event() for _ in sets]
-        for k in range(len(sets)):      # all slots start free
-            cmp_done[k].record(s_cmp)
-            out_done[k].record(s_out)
 
-        def e2e_step(i):
-            k = i % len(sets)
-            S = sets[k]
-            s_in.wait_event(cmp_done[k])            # the slot's inputs are no longer read
-            with torch.cuda.stream(s_in):
-                for d, h in zip(S["inputs"], hin):
-                    d.copy_(h, non_blocking=True)
-                in_done[k].record(s_in)
-            s_cmp.wait_event(in_done[k])
-            s_cmp.wait_event(out_done[k])           # the slot's outputs have been read back
-            with torch.cuda.stream(s_cmp):
-                for p_ in S["parts"]:
-                    p_.fn()
-                cmp_done[k].record(s_cmp)
-            s_out.wait_event(cmp_done[k])
-            with torch.cuda.stream(s_out):
-                for d, h in zip(S["outputs"], hout[k]):
-                    h.copy_(d, non_blocking=True)
-                out_done[k].record(s_out)
-
-        for i in range(max(2, args.warmup)):
-            e2e_step(i)
-        torch.cuda.synchronize()
-        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        e2e_steps = max(2, min(args.steps, 200))
-        if pg:
-            pg.barrier()
-        e0.record(s_in)
-        for i in range(e2e_steps):
-            e2e_step(i)
-        s_out.wait_stream(s_in)
-        s_out.wait_stream(s_cmp)
-        e1.record(s_out)
-        torch.cuda.synchronize()
-        if fg.device_status() != 0:
-            raise RuntimeError("device status after the end-to-end steps")
-        e2e_ms = e0.elapsed_time(e1) / e2e_steps
-        e2e = {"ms": e2e_ms, "h2d": sum(t.numel() * t.element_size() for t in W["inputs"]),
-               "d2h": sum(t.numel() * t.element_size() for t in W["outputs"])}
-        del sets
-
-    vals = reduce_max(part_ms + ([e2e["ms"]] if e2e else []), pg)
-    part_ms = vals[:n]
-    if e2e:
-        e2e["ms"] = vals[n]
-    ms_step = sum(part_ms)
-    value = world * W["flops"] / (ms_step * 1e-3) / 1e12
-
-    if rank != 0:
-        if pg:
-            pg.destroy_process_group()
-        return None
-
-    traffic = load_traffic(args.workload)
+def kernel_entries(parts, part_ms, traffic, hbm, fp8_peak):
+    """Per part: time, achieved rate against its roofline, DRAM traffic."""
     kernels = []
     for p_, ms in zip(parts, part_ms):
         if p_.bound == "hbm":
@@ -473,6 +443,147 @@ def run_ours(args):
             k["achieved_gbs"] = round(gbs, 1)
             k["frac_hbm"] = round(gbs / hbm, 4)
         kernels.append(k)
+    return kernels
+
+
+def e2e_run(W, args, dev, rank, fg, synth, pg):
+    """End to end through the public API: every step uploads its inputs from
+    pinned host memory, runs the step and reads its outputs back into
+    pinned host memory. Two copies of the workload's device buffers and
+    three streams let step i's upload, step i-1's kernels and step i-2's
+    read-back run at the same time (as a data loader feeding a training or
+    serving loop does); each step still moves all of its bytes."""
+    import torch
+    sets = [W, build(args.workload, dev, rank, fg, synth)]
+    hin = [t.cpu().pin_memory() for t in W["inputs"]]
+    hout = [[torch.empty(t.shape, dtype=t.dtype).pin_memory() for t in S["outputs"]] for S in sets]
+    s_in, s_cmp, s_out = torch.cuda.Stream(), torch.cuda.Stream(), torch.cuda.Stream()
+    in_done = [torch.cuda.Event() for _ in sets]
+    cmp_done = [torch.cuda.Event() for _ in sets]
+    out_done = [torch.cuda.Event() for _ in sets]
+    for k in range(len(sets)):      # all slots start free
+        cmp_done[k].record(s_cmp)
+        out_done[k].record(s_out)
+
+    def e2e_step(i):
+        k = i % len(sets)
+        S = sets[k]
+        s_in.wait_event(cmp_done[k])            # the slot's inputs are no longer read
+        with torch.cuda.stream(s_in):
+            for d, h in zip(S["inputs"], hin):
+                d.copy_(h, non_blocking=True)
+            in_done[k].record(s_in)
+        s_cmp.wait_event(in_done[k])
+        s_cmp.wait_event(out_done[k])           # the slot's outputs have been read back
+        with torch.cuda.stream(s_cmp):
+            for p_ in S["parts"]:
+                p_.fn()
+            cmp_done[k].record(s_cmp)
+        s_out.wait_event(cmp_done[k])
+        with torch.cuda.stream(s_out):
+            for d, h in zip(S["outputs"], hout[k]):
+                h.copy_(d, non_blocking=True)
+            out_done[k].record(s_out)
+
+    for i in range(max(2, args.warmup)):
+        e2e_step(i)
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e2e_steps = max(2, min(args.steps, 200))
+    if pg:
+        pg.barrier()
+    e0.record(s_in)
+    for i in range(e2e_steps):
+        e2e_step(i)
+    s_out.wait_stream(s_in)
+    s_out.wait_stream(s_cmp)
+    e1.record(s_out)
+    torch.cuda.synchronize()
+    if fg.device_status() != 0:
+        raise RuntimeError("device status after the end-to-end steps")
+    ms = reduce_max([e0.elapsed_time(e1) / e2e_steps], pg)[0]
+    del sets
+    return {"ms": ms, "h2d": sum(t.numel() * t.element_size() for t in W["inputs"]),
+            "d2h": sum(t.numel() * t.element_size() for t in W["outputs"])}
+
+
+# the five workloads of the measurement plan; the headline is one of them,
+# the others are reported under "configs" on the same line
+CONFIG_SET = ("tiny", "dense", "trio", "moe", "outliers")
+
+
+def run_ours(args):
+    import torch
+
+    import fp8_fine_grained_gb300 as fg
+    from fp8_fine_grained_gb300 import synth
+
+    world, rank, local = dist_env()
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    pg = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl")
+        pg = dist
+
+    hbm, bf16, peak_kind = peaks()
+    fp8_peak = 2.0 * bf16   # nominal FP8/BF16 dense ratio 4.5/2.25 on the measured BF16 burst
+    flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
+    clean = torch.ones(L2_CLEAN_BYTES // 4, dtype=torch.float32, device=dev)
+    sink = torch.empty((), dtype=torch.float32, device=dev)
+    stream = torch.cuda.current_stream()
+
+    def flush_l2():
+        flush.zero_()
+        torch.sum(clean, dim=0, out=sink)
+
+    clocks = ClockSampler(local, args.clock_log)
+    W = build(args.workload, dev, rank, fg, synth)
+    parts = W["parts"]
+    flops, dims = W["flops"], W["dims"]
+    n = len(parts)
+    with clocks:
+        part_ms, region = time_parts(W, args, pg, clocks, stream, flush_l2)
+    clk = clocks.summary(region)
+
+    e2e = e2e_run(W, args, dev, rank, fg, synth, pg) if args.workload in WORKLOADS else None
+    ms_step = sum(part_ms)
+    value = world * flops / (ms_step * 1e-3) / 1e12
+
+    # the other workloads of the measurement plan, each timed the same way
+    configs = {}
+    if not args.headline_only and args.workload in CONFIG_SET:
+        del W
+        torch.cuda.empty_cache()
+        for name in CONFIG_SET:
+            if name == args.workload:
+                continue
+            Wc = build(name, dev, rank, fg, synth)
+            cclk = ClockSampler(local)
+            with cclk:
+                cms, creg = time_parts(Wc, args, pg, cclk, stream, flush_l2)
+            kern = kernel_entries(Wc["parts"], cms, load_traffic(name), hbm, fp8_peak)
+            dom = max(range(len(cms)), key=lambda j: cms[j])
+            configs[name] = {"workload": WORKLOADS[name], "ms_per_step": round(sum(cms), 4),
+                             "value": round(world * Wc["flops"] / (sum(cms) * 1e-3) / 1e12, 2),
+                             "unit": "TFLOP/s", "dims": Wc["dims"],
+                             "roofline": {k: kern[dom][k] for k in ("kernel", "bound", "achieved", "peak", "unit",
+                                                                    "frac", "traffic")},
+                             "kernels": kern, "clocks": cclk.summary(creg),
+                             "gpu_launches": len(Wc["parts"]) * args.steps}
+            cclk.cleanup()
+            del Wc
+            torch.cuda.empty_cache()
+    clocks.cleanup()
+
+    if rank != 0:
+        if pg:
+            pg.destroy_process_group()
+        return None
+
+    traffic = load_traffic(args.workload)
+    kernels = kernel_entries(parts, part_ms, traffic, hbm, fp8_peak)
     dom = max(range(n), key=lambda j: part_ms[j])
     dk = kernels[dom]
     roofline = {"bound": dk["bound"], "kernel": dk["kernel"], "achieved": dk["achieved"], "peak": dk["peak"],
@@ -495,27 +606,36 @@ def run_ours(args):
         "vs_baseline": None,
         "dtype": "e4m3 x e4m3 -> f32 accumulate",
         "data": "synthetic (seeded torch Philox; shapes and distributions of the workload)",
-        "config": dict({"workload": WORKLOADS[args.workload],
-                        "l2": "flushed between steps (512 MiB write + 256 MiB read, outside the timed region)",
-                        "parallelism": "replica per GPU" if world > 1 else "single GPU"}, **W["dims"]),
+        "config": config_of(args.workload, world),
+        "dims": dims,
         "roofline": roofline,
         "quant": quant,
         "kernels": kernels,
-        "clocks": clocks.summary(),
+        "clocks": clk,
         "gpu_launches": n * args.steps,
     }
     if e2e:
-        line["e2e"] = {"value": round(world * W["flops"] / (e2e["ms"] * 1e-3) / 1e12, 2), "unit": "TFLOP/s",
-                       "h2d_bytes_per_step": e2e["h2d"], "d2h_bytes_per_step": e2e["d2h"],
+        line["e2e"] = {"value": round(world * flops / (e2e["ms"] * 1e-3) / 1e12, 2),
+                       "unit": "TFLOP/s", "h2d_bytes_per_step": e2e["h2d"], "d2h_bytes_per_step": e2e["d2h"],
                        "ms_per_step": round(e2e["ms"], 4),
                        "pipeline": "upload, kernels and read-back of consecutive steps overlap "
                                    "(two buffer sets, three streams)"}
+    if configs:
+        line["configs"] = configs
     if not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(args.workload, budget_s=args.cpu_seconds)
     print(json.dumps(line), flush=True)
     if pg:
         pg.destroy_process_group()
     return line
+
+
+def config_of(workload, world):
+    """The workload's config object, printed identically by both arms."""
+    M, K, N = oracle_dims(workload)
+    return {"workload": WORKLOADS[workload],
+            "l2": "flushed between steps (512 MiB write + 256 MiB read, outside the timed region)",
+            "parallelism": "replica per GPU" if world > 1 else "single GPU", "M": M, "K": K, "N": N}
 
 
 # -------------------------------------------------------------- CPU oracle ----
@@ -600,7 +720,7 @@ def run_reference(args):
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms, 3), "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "e4m3 x e4m3 -> f64 block sums, f32 accumulate",
         "data": "synthetic (seeded)",
-        "config": {"workload": WORKLOADS[args.workload], "M": M, "K": K, "N": N},
+        "config": config_of(args.workload, world),
         "cpu_baseline": {"value": round(value, 6), "unit": "TFLOP/s", "cores": th, "kind": "oracle",
                          "sample": "per step %d of %d rows of X, quantised and multiplied by the full W" % (rows, M)},
         "e2e": {"value": round(value, 6), "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
@@ -618,6 +738,10 @@ def main():
     ap.add_argument("--workload", choices=sorted(WORKLOADS), default="dense")
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--headline-only", action="store_true",
+                    help="time only --workload (skip the other workloads under \"configs\")")
+    ap.add_argument("--clock-log", default=None,
+                    help="keep the nvidia-smi clock samples in this file (default: a temporary file)")
     args = ap.parse_args()
     if args.impl == "reference":
         args.steps = 3 if args.steps is None else args.steps

@@ -94,15 +94,125 @@ def _ptr(t):
     return ctypes.c_void_p(t.data_ptr()) if t is not None else None
 
 
-def _rowmajor(t, name):
+def _layout(t, name):
     if t.dim() != 2 or t.stride(1) != 1:
         raise ValueError("%s must be a 2-D row-major tensor (unit inner stride)" % name)
-    if not t.is_cuda:
-        raise ValueError("%s must be a CUDA tensor" % name)
+
+
+def _on_gpu(*named):
+    for t, name in named:
+        if t is not None and not t.is_cuda:
+            raise ValueError("%s must be a CUDA tensor" % name)
+
+
+def _rowmajor(t, name):
+    _layout(t, name)
+    _on_gpu((t, name))
 
 
 def _pad(n, m):
     return (n + m - 1) // m * m
+
+
+def _dtype(t, dtype, name):
+    if t.dtype != dtype:
+        raise ValueError("%s must be %s, got %s" % (name, dtype, t.dtype))
+
+
+def _at_least(t, rows, cols, name):
+    """A 2-D tensor must cover [rows, cols] (the kernels read or write that
+    extent through raw pointers, so a smaller tensor would be overrun)."""
+    if t.dim() != 2 or t.shape[0] < rows or t.shape[1] < cols:
+        raise ValueError("%s must cover [%d, %d], got %s" % (name, rows, cols, tuple(t.shape)))
+
+
+def _quant_out(q, scales, q_shape, s_rows, s_cols, qn="q", sn="scales"):
+    """Caller-supplied outputs of a quantiser: E4M3 bytes of q_shape and
+    FP32 scales covering [s_rows, s_cols]."""
+    torch = _torch()
+    _dtype(q, torch.uint8, qn)
+    _dtype(scales, torch.float32, sn)
+    _layout(q, qn)
+    _layout(scales, sn)
+    _at_least(q, q_shape[0], q_shape[1], qn)
+    _at_least(scales, s_rows, s_cols, sn)
+
+
+def _gemm_operands(mode, a, sa, b, sb):
+    """Dtypes and extents of a block-scaled GEMM's operands; returns (M, N, K).
+
+    FPROP: a [M,K], sa [K/128, >=M], b [N,K], sb [N/128, K/128]
+    DGRAD: a [M,K], sa [K/128, >=M], b [K,N], sb [K/128, N/128]
+    WGRAD: a [M,K], sa [K/128, >=M], b [N,K], sb [K/128, >=N]
+    """
+    torch = _torch()
+    if mode not in (FPROP, DGRAD, WGRAD):
+        raise ValueError("mode must be FPROP, DGRAD or WGRAD")
+    for t, n in ((a, "a"), (b, "b"), (sa, "sa"), (sb, "sb")):
+        _layout(t, n)
+    _dtype(a, torch.uint8, "a")
+    _dtype(b, torch.uint8, "b")
+    _dtype(sa, torch.float32, "sa")
+    _dtype(sb, torch.float32, "sb")
+    M, K = a.shape
+    if mode == DGRAD:
+        if b.shape[0] != K:
+            raise ValueError("dgrad: b must be [K, N] with K = a.shape[1] = %d, got %s" % (K, tuple(b.shape)))
+        N = b.shape[1]
+    else:
+        if b.shape[1] != K:
+            raise ValueError("b must be [N, K] with K = a.shape[1] = %d, got %s" % (K, tuple(b.shape)))
+        N = b.shape[0]
+    kb = K // 128
+    _at_least(sa, kb, M, "sa")
+    if mode == FPROP:
+        _at_least(sb, N // 128, kb, "sb")
+    elif mode == DGRAD:
+        _at_least(sb, kb, N // 128, "sb")
+    else:
+        _at_least(sb, kb, N, "sb")
+    return M, N, K
+
+
+def _gemm_out(c, M, N):
+    _layout(c, "c")
+    if tuple(c.shape) != (M, N):
+        raise ValueError("c must be [%d, %d], got %s" % (M, N, tuple(c.shape)))
+
+
+def _grouped_operands(xq, sx, expert_offsets, wq, sw, n_rows, row_index):
+    """Dtypes and extents of a grouped GEMM's operands; returns (T, E, N, K)."""
+    torch = _torch()
+    _layout(xq, "xq")
+    _layout(sx, "sx")
+    _dtype(xq, torch.uint8, "xq")
+    _dtype(sx, torch.float32, "sx")
+    _dtype(wq, torch.uint8, "wq")
+    _dtype(sw, torch.float32, "sw")
+    if expert_offsets.dtype != torch.int32 or (row_index is not None and row_index.dtype != torch.int32):
+        raise ValueError("row_index and expert_offsets must be int32")
+    if not ((row_index is None or row_index.is_contiguous()) and expert_offsets.is_contiguous()
+            and wq.is_contiguous() and sw.is_contiguous()):
+        raise ValueError("row_index, expert_offsets, wq, sw must be contiguous")
+    if wq.dim() != 3:
+        raise ValueError("wq must be [E, N, K]")
+    T, K = xq.shape
+    E, N, K2 = wq.shape
+    if K2 != K or xq.stride(0) != K:
+        raise ValueError("xq must be [T, K] contiguous with the experts' K")
+    if n_rows < 0:
+        raise ValueError("n_rows must be >= 0")
+    if expert_offsets.dim() != 1 or expert_offsets.numel() != E + 1:
+        raise ValueError("expert_offsets must hold E + 1 = %d entries" % (E + 1))
+    if tuple(sw.shape) != (E, N // 128, K // 128):
+        raise ValueError("sw must be [%d, %d, %d], got %s" % (E, N // 128, K // 128, tuple(sw.shape)))
+    _at_least(sx, K // 128, T, "sx")
+    if row_index is None:
+        if T < n_rows:
+            raise ValueError("without a row index xq and sx must hold n_rows = %d rows" % n_rows)
+    elif row_index.dim() != 1 or row_index.numel() < n_rows:
+        raise ValueError("row_index must hold n_rows = %d entries" % n_rows)
+    return T, E, N, K
 
 
 # ------------------------------------------------------------- quantise ----
@@ -118,7 +228,7 @@ def fp8_quant_1x128(x, transpose=False, q=None, scales=None, stream=None, pow2=F
         (rows % 128 == 0); returns q uint8 [cols, rows], scales [rows/128, ld_s>=cols].
     """
     torch = _torch()
-    _rowmajor(x, "x")
+    _layout(x, "x")
     if x.dtype != torch.bfloat16:
         raise ValueError("x must be bfloat16")
     rows, cols = x.shape
@@ -127,11 +237,14 @@ def fp8_quant_1x128(x, transpose=False, q=None, scales=None, stream=None, pow2=F
             q = torch.empty((rows, cols), dtype=torch.uint8, device=x.device)
         if scales is None:
             scales = torch.empty((cols // 128, _pad(max(rows, 1), 4)), dtype=torch.float32, device=x.device)
+        _quant_out(q, scales, (rows, cols), cols // 128, rows)
     else:
         if q is None:
             q = torch.empty((cols, rows), dtype=torch.uint8, device=x.device)
         if scales is None:
             scales = torch.empty((rows // 128, _pad(max(cols, 1), 4)), dtype=torch.float32, device=x.device)
+        _quant_out(q, scales, (cols, rows), rows // 128, cols)
+    _on_gpu((x, "x"), (q, "q"), (scales, "scales"))
     fn = lib().fp8_quant_1x128_pow2 if pow2 else lib().fp8_quant_1x128
     rc = fn(_ptr(x), rows, cols, x.stride(0), _ptr(q), q.stride(0), _ptr(scales),
             scales.stride(0), 1 if transpose else 0, _stream(stream))
@@ -145,7 +258,7 @@ def fp8_quant_1x128_dual(x, q=None, scales=None, qT=None, scalesT=None, stream=N
     fp8_quant_1x128(x) and fp8_quant_1x128(x, transpose=True) (with the
     same pow2 choice)."""
     torch = _torch()
-    _rowmajor(x, "x")
+    _layout(x, "x")
     if x.dtype != torch.bfloat16:
         raise ValueError("x must be bfloat16")
     rows, cols = x.shape
@@ -158,6 +271,9 @@ def fp8_quant_1x128_dual(x, q=None, scales=None, qT=None, scalesT=None, stream=N
         qT = torch.empty((cols, rows), dtype=torch.uint8, device=dev)
     if scalesT is None:
         scalesT = torch.empty((rows // 128, _pad(max(cols, 1), 4)), dtype=torch.float32, device=dev)
+    _quant_out(q, scales, (rows, cols), cols // 128, rows)
+    _quant_out(qT, scalesT, (cols, rows), rows // 128, cols, "qT", "scalesT")
+    _on_gpu((x, "x"), (q, "q"), (scales, "scales"), (qT, "qT"), (scalesT, "scalesT"))
     fn = lib().fp8_quant_1x128_dual_pow2 if pow2 else lib().fp8_quant_1x128_dual
     rc = fn(_ptr(x), rows, cols, x.stride(0), _ptr(q), q.stride(0), _ptr(scales),
             scales.stride(0), _ptr(qT), qT.stride(0), _ptr(scalesT), scalesT.stride(0),
@@ -172,7 +288,7 @@ def fp8_quant_1x128_gather(x, row_index, q=None, scales=None, stream=None, pow2=
     float32 [cols/128, ld_s>=n_rows]. Equal to gathering the rows of
     fp8_quant_1x128(x); feeds fp8_grouped_gemm with row_index=None."""
     torch = _torch()
-    _rowmajor(x, "x")
+    _layout(x, "x")
     if x.dtype != torch.bfloat16:
         raise ValueError("x must be bfloat16")
     if row_index.dtype != torch.int32 or not row_index.is_contiguous():
@@ -183,6 +299,8 @@ def fp8_quant_1x128_gather(x, row_index, q=None, scales=None, stream=None, pow2=
         q = torch.empty((rows, cols), dtype=torch.uint8, device=x.device)
     if scales is None:
         scales = torch.empty((cols // 128, _pad(max(rows, 1), 4)), dtype=torch.float32, device=x.device)
+    _quant_out(q, scales, (rows, cols), cols // 128, rows)
+    _on_gpu((x, "x"), (row_index, "row_index"), (q, "q"), (scales, "scales"))
     fn = lib().fp8_quant_1x128_gather_pow2 if pow2 else lib().fp8_quant_1x128_gather
     rc = fn(_ptr(x), n_src, cols, x.stride(0), _ptr(row_index), rows, _ptr(q),
             q.stride(0), _ptr(scales), scales.stride(0), _stream(stream))
@@ -196,7 +314,7 @@ def fp8_quant_1x128_scatter(x, dest_index, n_out, q=None, scales=None, stream=No
     q uint8 [n_out, cols], scales float32 [cols/128, ld_s>=n_out]. Equal to
     fp8_quant_1x128_gather with the inverse index; each row is read once."""
     torch = _torch()
-    _rowmajor(x, "x")
+    _layout(x, "x")
     if x.dtype != torch.bfloat16:
         raise ValueError("x must be bfloat16")
     if dest_index.dtype != torch.int32 or not dest_index.is_contiguous() or dest_index.dim() != 2:
@@ -209,6 +327,8 @@ def fp8_quant_1x128_scatter(x, dest_index, n_out, q=None, scales=None, stream=No
         q = torch.empty((n_out, cols), dtype=torch.uint8, device=x.device)
     if scales is None:
         scales = torch.empty((cols // 128, _pad(max(n_out, 1), 4)), dtype=torch.float32, device=x.device)
+    _quant_out(q, scales, (n_out, cols), cols // 128, n_out)
+    _on_gpu((x, "x"), (dest_index, "dest_index"), (q, "q"), (scales, "scales"))
     fn = lib().fp8_quant_1x128_scatter_pow2 if pow2 else lib().fp8_quant_1x128_scatter
     rc = fn(_ptr(x), n_src, cols, x.stride(0), _ptr(dest_index), k, n_out, _ptr(q), q.stride(0), _ptr(scales),
             scales.stride(0), _stream(stream))
@@ -222,7 +342,7 @@ def fp8_quant_128x128(w, q=None, scales=None, stream=None, pow2=False):
     torch = _torch()
     shape = w.shape
     w2 = w.reshape(-1, shape[-1]) if w.dim() == 3 else w
-    _rowmajor(w2, "w")
+    _layout(w2, "w")
     if w.dtype != torch.bfloat16:
         raise ValueError("w must be bfloat16")
     N, K = w2.shape
@@ -232,6 +352,12 @@ def fp8_quant_128x128(w, q=None, scales=None, stream=None, pow2=False):
         scales = torch.empty(tuple(shape[:-2]) + (shape[-2] // 128, K // 128), dtype=torch.float32,
                              device=w.device)
     q2 = q.reshape(-1, K)
+    _dtype(q, torch.uint8, "q")
+    _dtype(scales, torch.float32, "scales")
+    if tuple(q2.shape) != (N, K) or not q2.is_contiguous() or not scales.is_contiguous() \
+            or scales.numel() < (N // 128) * (K // 128):
+        raise ValueError("q must be %s uint8 and scales hold [N/128, K/128] float32" % (tuple(shape),))
+    _on_gpu((w2, "w"), (q, "q"), (scales, "scales"))
     fn = lib().fp8_quant_128x128_pow2 if pow2 else lib().fp8_quant_128x128
     rc = fn(_ptr(w2), N, K, w2.stride(0), _ptr(q2), q2.stride(0), _ptr(scales), _stream(stream))
     _check(rc, "fp8_quant_128x128_pow2" if pow2 else "fp8_quant_128x128")
@@ -257,15 +383,13 @@ def fp8_gemm_blockscaled(mode, a, sa, b, sb, out_dtype=None, c=None, stream=None
     WGRAD: a [M,K] + sa [K/128, >=M]; b [N,K] + sb [K/128, >=N] (both grouped along K) -> C [M,N]
     """
     torch = _torch()
-    for t, n in ((a, "a"), (b, "b"), (sa, "sa"), (sb, "sb")):
-        _rowmajor(t, n)
-    M, K = a.shape
-    N = b.shape[1] if mode == DGRAD else b.shape[0]
+    M, N, K = _gemm_operands(mode, a, sa, b, sb)
     if out_dtype is None:
         out_dtype = torch.float32 if mode == WGRAD else torch.bfloat16
     if c is None:
         c = torch.empty((M, N), dtype=out_dtype, device=a.device)
-    _rowmajor(c, "c")
+    _gemm_out(c, M, N)
+    _on_gpu((a, "a"), (b, "b"), (sa, "sa"), (sb, "sb"), (c, "c"))
     rc = lib().fp8_gemm_blockscaled(mode, _ptr(a), _ptr(sa), a.stride(0), sa.stride(0), _ptr(b), _ptr(sb),
                                     b.stride(0), sb.stride(0), M, N, K, _ptr(c), _out_code(c.dtype),
                                     c.stride(0), _stream(stream))
@@ -278,15 +402,13 @@ def fp8_gemm_mx(mode, a, sa, b, sb, out_dtype=None, c=None, stream=None):
     quantisers' output), with the scales applied by the tensor cores'
     block-scaled MMA; same modes, shapes and layouts."""
     torch = _torch()
-    for t, n in ((a, "a"), (b, "b"), (sa, "sa"), (sb, "sb")):
-        _rowmajor(t, n)
-    M, K = a.shape
-    N = b.shape[1] if mode == DGRAD else b.shape[0]
+    M, N, K = _gemm_operands(mode, a, sa, b, sb)
     if out_dtype is None:
         out_dtype = torch.float32 if mode == WGRAD else torch.bfloat16
     if c is None:
         c = torch.empty((M, N), dtype=out_dtype, device=a.device)
-    _rowmajor(c, "c")
+    _gemm_out(c, M, N)
+    _on_gpu((a, "a"), (b, "b"), (sa, "sa"), (sb, "sb"), (c, "c"))
     rc = lib().fp8_gemm_mx(mode, _ptr(a), _ptr(sa), a.stride(0), sa.stride(0), _ptr(b), _ptr(sb),
                            b.stride(0), sb.stride(0), M, N, K, _ptr(c), _out_code(c.dtype),
                            c.stride(0), _stream(stream))
@@ -299,15 +421,19 @@ def fp8_gemm_blockscaled_e4m3(mode, a, sa, b, sb, c=None, scales=None, stream=No
     (C E4M3 [M,N], scales [N/128, ld_s>=M]), equal to fp8_quant_1x128 of
     the bf16 output of fp8_gemm_blockscaled."""
     torch = _torch()
-    for t, n in ((a, "a"), (b, "b"), (sa, "sa"), (sb, "sb")):
-        _rowmajor(t, n)
-    M, K = a.shape
-    N = b.shape[1] if mode == DGRAD else b.shape[0]
+    if mode not in (FPROP, DGRAD):
+        raise ValueError("the E4M3 output exists for FPROP and DGRAD only")
+    M, N, K = _gemm_operands(mode, a, sa, b, sb)
     if c is None:
         c = torch.empty((M, N), dtype=torch.uint8, device=a.device)
     if scales is None:
         scales = torch.empty((N // 128, _pad(max(M, 1), 4)), dtype=torch.float32, device=a.device)
-    _rowmajor(c, "c")
+    _dtype(c, torch.uint8, "c")
+    _gemm_out(c, M, N)
+    _dtype(scales, torch.float32, "scales")
+    _layout(scales, "scales")
+    _at_least(scales, N // 128, M, "scales")
+    _on_gpu((a, "a"), (b, "b"), (sa, "sa"), (sb, "sb"), (c, "c"), (scales, "scales"))
     rc = lib().fp8_gemm_blockscaled_e4m3(mode, _ptr(a), _ptr(sa), a.stride(0), sa.stride(0), _ptr(b), _ptr(sb),
                                          b.stride(0), sb.stride(0), M, N, K, _ptr(c), c.stride(0), _ptr(scales),
                                          scales.stride(0), _stream(stream))
@@ -339,22 +465,15 @@ def fp8_grouped_gemm(xq, sx, row_index, expert_offsets, wq, sw, n_rows, out_dtyp
     from fp8_quant_1x128_gather), row r of xq feeds output row r (T >= n_rows).
     """
     torch = _torch()
-    _rowmajor(xq, "xq")
-    _rowmajor(sx, "sx")
-    if expert_offsets.dtype != torch.int32 or (row_index is not None and row_index.dtype != torch.int32):
-        raise ValueError("row_index and expert_offsets must be int32")
-    if not ((row_index is None or row_index.is_contiguous()) and expert_offsets.is_contiguous()
-            and wq.is_contiguous() and sw.is_contiguous()):
-        raise ValueError("row_index, expert_offsets, wq, sw must be contiguous")
-    T, K = xq.shape
-    E, N, K2 = wq.shape
-    if K2 != K or xq.stride(0) != K:
-        raise ValueError("xq must be [T, K] contiguous with the experts' K")
+    T, E, N, K = _grouped_operands(xq, sx, expert_offsets, wq, sw, n_rows, row_index)
     if out_dtype is None:
         out_dtype = torch.bfloat16
     if y is None:
         y = torch.empty((n_rows, N), dtype=out_dtype, device=xq.device)
-    _rowmajor(y, "y")
+    _layout(y, "y")
+    _at_least(y, n_rows, N, "y")
+    _on_gpu((xq, "xq"), (sx, "sx"), (wq, "wq"), (sw, "sw"), (expert_offsets, "expert_offsets"),
+            (row_index, "row_index"), (y, "y"))
     ri = None if row_index is None else _ptr(row_index)
     rc = lib().fp8_grouped_gemm(_ptr(xq), _ptr(sx), sx.stride(0), T, ri, _ptr(expert_offsets), E,
                                 n_rows, _ptr(wq), _ptr(sw), N, K, _ptr(y), _out_code(y.dtype), y.stride(0),
@@ -367,23 +486,14 @@ def fp8_grouped_gemm_mx(xq, sx, expert_offsets, wq, sw, n_rows, out_dtype=None, 
     """fp8_grouped_gemm with rows already in expert order (row_index=None)
     for power-of-two scales, on the tensor cores' block-scaled MMA."""
     torch = _torch()
-    _rowmajor(xq, "xq")
-    _rowmajor(sx, "sx")
-    if not (wq.is_contiguous() and sw.is_contiguous()):
-        raise ValueError("wq and sw must be contiguous")
-    if expert_offsets.dtype != torch.int32 or not expert_offsets.is_contiguous():
-        raise ValueError("expert_offsets must be contiguous int32")
-    E, N, K = wq.shape
-    T, K2 = xq.shape
-    if K2 != K or xq.stride(0) != K:
-        raise ValueError("xq must be [n_rows, K] contiguous with the experts' K")
-    if T < n_rows or sx.shape[1] < n_rows:
-        raise ValueError("xq and sx must hold n_rows rows")
+    T, E, N, K = _grouped_operands(xq, sx, expert_offsets, wq, sw, n_rows, None)
     if out_dtype is None:
         out_dtype = torch.bfloat16
     if y is None:
         y = torch.empty((n_rows, N), dtype=out_dtype, device=xq.device)
-    _rowmajor(y, "y")
+    _layout(y, "y")
+    _at_least(y, n_rows, N, "y")
+    _on_gpu((xq, "xq"), (sx, "sx"), (wq, "wq"), (sw, "sw"), (expert_offsets, "expert_offsets"), (y, "y"))
     rc = lib().fp8_grouped_gemm_mx(_ptr(xq), _ptr(sx), sx.stride(0), _ptr(expert_offsets), E, n_rows, _ptr(wq),
                                    _ptr(sw), N, K, _ptr(y), _out_code(y.dtype), y.stride(0), _stream(stream))
     _check(rc, "fp8_grouped_gemm_mx")

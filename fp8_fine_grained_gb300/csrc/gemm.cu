@@ -12,7 +12,12 @@
 // GB300 design (one CTA per SM, persistent over 128x256 output tiles):
 //   warp 0      TMA producer: A tile 128x128 B and B tile 256x128 B per
 //               contraction block into a 4-stage shared-memory ring
-//               (128-byte swizzle), signalled on mbarriers.
+//               (128-byte swizzle), signalled on mbarriers. The block's
+//               dequantisation scales travel in the same stage: the tile's
+//               128 row scales (and, for the weight gradient, its 256 column
+//               scales) by TMA, the two 128x128 weight-block scales by 4-byte
+//               cp.async, so the promotion warps read them from shared memory
+//               instead of waiting on L2 once per block.
 //   warp 1      MMA issuer: allocates all 512 tensor-memory columns, issues
 //               4 x tcgen05.mma (M128 N256 K32, E4M3 -> FP32) per block into
 //               one of two 256-column TMEM partial buffers, and commits to
@@ -22,7 +27,8 @@
 //               complete warpgroup 0 so that setmaxnreg can move its
 //               registers to the promotion warpgroups).
 //   warps 4..11 promotion/epilogue: each thread owns one output row and 128
-//               columns; per block it loads the partial from TMEM
+//               columns; per block it reads its scales from the stage, loads
+//               the partial from TMEM
 //               (tcgen05.ld 32x32b, 32 columns at a time, two loads in
 //               flight), does acc = fma(P, sA*sB, acc) in FP32 registers
 //               (paired FP32 FMAs) and frees the TMEM buffer, so the MMA of
@@ -50,7 +56,7 @@ constexpr int STAGES = 4;
 constexpr int EPI_WARPS = 8;
 constexpr int EPI_WARP0 = 4;                  // promotion warps are warpgroups 1 and 2
 constexpr int NUM_THREADS = (EPI_WARP0 + EPI_WARPS) * 32;
-constexpr int CHUNK = 32;                     // TMEM columns per tcgen05.ld in the promotion loop
+constexpr int CHUNK = 16;                     // TMEM columns per tcgen05.ld in the promotion loop
 // Register split (setmaxnreg): warpgroup 0 (TMA, MMA and two idle warps)
 // gives registers to the two promotion warpgroups, which hold 128 FP32 sums
 // per thread plus two 32-column partial buffers. The launch holds
@@ -108,7 +114,26 @@ struct Params {
     int64_t ld_sC;
 };
 
-struct SmemLayout {
+// Scale slot of one pipeline stage: the A row scales of the block (a box of
+// 132 FP32 from the 4-aligned row at or below the tile's first row, so that
+// the TMA start coordinate is 16-byte aligned; the tile's rows begin at
+// offset m0 % 4), then the B scales: the two 128x128 weight-block scales of
+// the tile's column halves, or (weight gradient) the tile's 256 column scales.
+// Gathered MoE rows receive their row scales by cp.async instead (128 FP32,
+// one per tile row).
+constexpr uint32_t SA_BOX = 132;
+template <int MODE> struct ScaleSlot {
+    static constexpr uint32_t a_bytes = MODE == GROUPED ? 4 * BM : 4 * SA_BOX;
+    static constexpr uint32_t b_off = MODE == WGRAD ? 640 : a_bytes;              // TMA destination: 128-byte aligned
+    static constexpr uint32_t b_bytes = MODE == WGRAD ? 4 * BN : 16;
+    static constexpr uint32_t bytes = MODE == GROUPED ? b_off + b_bytes : (b_off + b_bytes + 127) / 128 * 128;
+};
+
+// Shared memory, from a 1024-byte aligned base (the 128-byte swizzle atoms of
+// the operand stages need it): B stages, A stages, barriers, the promotion
+// warps' epilogue staging blocks, the stages' scale slots and, for MoE
+// experts, the tile's token rows and the experts' tile prefix.
+template <int MODE> struct SmemLayout {
     // B stages first: every operand read stays well inside the allocation
     static constexpr uint32_t b_off = 0;
     static constexpr uint32_t a_off = b_off + STAGES * B_STAGE_BYTES;
@@ -120,17 +145,31 @@ struct SmemLayout {
     static constexpr uint32_t tmem_ptr_off = tempty_off + 8 * 2;
     static constexpr uint32_t abort_off = tmem_ptr_off + 4;
     static constexpr uint32_t misc_end = abort_off + 4;
-    // per promotion warp: epilogue staging block; during the main loop its
-    // first 512 bytes hold the warp's 128 WGRAD column scales of the block
+    // per promotion warp: epilogue staging block
     static constexpr uint32_t stage_c_off = (misc_end + 15) & ~15u;
     static constexpr uint32_t stage_c_end = stage_c_off + EPI_WARPS * STAGE_C_BYTES;
-    static constexpr uint32_t tok_off = stage_c_end;                      // GROUPED: the tile's token rows
-    static constexpr uint32_t tok_end = tok_off + 4 * BM;
-    static constexpr uint32_t prefix_off = tok_end;                       // GROUPED tile prefix
-    static constexpr uint32_t prefix_end = prefix_off + 4 * (MAX_EXPERTS + 1);
-    static constexpr uint32_t total = prefix_end + 1024;                 // + alignment slack
+    static constexpr uint32_t scale_off = (stage_c_end + 127) & ~127u;
+    static constexpr uint32_t scale_end = scale_off + STAGES * ScaleSlot<MODE>::bytes;
+    static constexpr uint32_t tok_off = scale_end;                              // GROUPED: the tile's token rows
+    static constexpr uint32_t tok_end = tok_off + (MODE == GROUPED ? 4 * BM : 0);
+    static constexpr uint32_t prefix_off = tok_end;                             // grouped: tile prefix
+    static constexpr uint32_t prefix_end = prefix_off + (is_grouped(MODE) ? 4 * (MAX_EXPERTS + 1) : 0);
+    static constexpr uint32_t total = prefix_end;
 };
-static_assert(SmemLayout::total <= 232448, "shared memory budget");
+static_assert(SmemLayout<FPROP>::total <= 232448, "shared memory budget");
+static_assert(SmemLayout<WGRAD>::total <= 232448, "shared memory budget");
+static_assert(SmemLayout<GROUPED>::total <= 232448, "shared memory budget");
+static_assert(SmemLayout<GROUPED_C>::total <= 232448, "shared memory budget");
+
+// Arrivals that complete a stage's "full" barrier: the producer's
+// arrive.expect_tx; the completion of warp 2's 4-byte weight-scale copies
+// (fprop, dgrad, experts with rows in expert order; the weight gradient's
+// scales all come by TMA); or, for MoE rows gathered through a row index,
+// the two gather warps (whose copies include the weight-block scales).
+template <int MODE> constexpr uint32_t full_arrivals()
+{
+    return MODE == GROUPED ? 1 + GATHER_WARPS : (MODE == WGRAD ? 1 : 2);
+}
 
 struct Tile {
     int64_t m0;       // first A row (dense) / first output row (grouped)
@@ -138,6 +177,21 @@ struct Tile {
     int64_t n0;       // first output column
     int expert;
 };
+
+// Weight-block scale of column half h of tile tl for contraction block kb:
+// sB is [N/128][ld_sB] (fprop), [K/128][ld_sB] (dgrad) or
+// [E][N/128][K/128] (experts).
+template <int MODE>
+__device__ __forceinline__ const float *weight_scale(const Params &p, const Tile &tl, int kb, int h)
+{
+    const int64_t nb = tl.n0 / 128 + h;
+    if constexpr (MODE == FPROP)
+        return p.sB + nb * p.ld_sB + kb;
+    else if constexpr (MODE == DGRAD)
+        return p.sB + (int64_t)kb * p.ld_sB + nb;
+    else
+        return p.sB + ((int64_t)tl.expert * (p.N / 128) + nb) * (p.K / 128) + kb;
+}
 
 template <int MODE>
 __device__ __forceinline__ Tile decode_tile(int64_t t, const Params &p, const int32_t *prefix)
@@ -167,18 +221,29 @@ __device__ __forceinline__ Tile decode_tile(int64_t t, const Params &p, const in
 
 template <int MODE, int OUT>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
-    gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB, const Params p)
+    gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                const __grid_constant__ CUtensorMap tmSA, const __grid_constant__ CUtensorMap tmSB, const Params p)
 {
-    extern __shared__ uint8_t smem_raw[];
-    uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    using L = SmemLayout<MODE>;
+    using SS = ScaleSlot<MODE>;
+    extern __shared__ __align__(1024) uint8_t smem_raw[];
+    uint8_t *smem = smem_raw;
+    // the layout assumes the 1024-byte alignment requested above; refuse to
+    // run (before any barrier or tensor memory is set up) if it is missing
+    if (smem_u32(smem) & 1023u) {
+        if (threadIdx.x == 0)
+            atomicCAS(p.status, 0, FP8FG_EUNSUPPORTED);
+        return;
+    }
     const uint32_t sbase = smem_u32(smem);
-    const uint32_t full_bar = sbase + SmemLayout::full_off;
-    const uint32_t empty_bar = sbase + SmemLayout::empty_off;
-    const uint32_t tfull_bar = sbase + SmemLayout::tfull_off;
-    const uint32_t tempty_bar = sbase + SmemLayout::tempty_off;
-    volatile uint32_t *tmem_ptr = reinterpret_cast<volatile uint32_t *>(smem + SmemLayout::tmem_ptr_off);
-    volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + SmemLayout::abort_off);
-    int32_t *prefix = reinterpret_cast<int32_t *>(smem + SmemLayout::prefix_off);
+    const uint32_t full_bar = sbase + L::full_off;
+    const uint32_t empty_bar = sbase + L::empty_off;
+    const uint32_t tfull_bar = sbase + L::tfull_off;
+    const uint32_t tempty_bar = sbase + L::tempty_off;
+    volatile uint32_t *tmem_ptr = reinterpret_cast<volatile uint32_t *>(smem + L::tmem_ptr_off);
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + L::abort_off);
+    int32_t *prefix = reinterpret_cast<int32_t *>(smem + L::prefix_off);
+    const uint32_t scale_base = sbase + L::scale_off;
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
@@ -189,8 +254,11 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < STAGES; ++s) {
-            mbar_init(full_bar + 8 * s, gathered ? 1 + GATHER_WARPS : 1);
-            mbar_init(empty_bar + 8 * s, 1);
+            mbar_init(full_bar + 8 * s, full_arrivals<MODE>());
+            // freed by the MMA's commit and by every promotion warp once it
+            // has read the stage's scales (before it waits for the block's
+            // partial, so refills are not held back by the fold)
+            mbar_init(empty_bar + 8 * s, 1 + EPI_WARPS);
         }
         for (int b = 0; b < 2; ++b) {
             mbar_init(tfull_bar + 8 * b, 1);
@@ -200,13 +268,18 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         fence_mbar_init();
         tma_prefetch_desc(&tmA);
         tma_prefetch_desc(&tmB);
+        if constexpr (!gathered)
+            tma_prefetch_desc(&tmSA);
+        if constexpr (MODE == WGRAD)
+            tma_prefetch_desc(&tmSB);
     }
     if (warp == 1) {
-        tmem_alloc(sbase + SmemLayout::tmem_ptr_off, TMEM_COLS);
+        tmem_alloc(sbase + L::tmem_ptr_off, TMEM_COLS);
         tmem_relinquish();
     }
     if constexpr (is_grouped(MODE))
-        build_group_prefix<NUM_THREADS>(p.expert_offsets, p.n_experts, p.n_rows, p.num_n_tiles, BM, p.status, prefix);
+        build_group_prefix<NUM_THREADS>(p.expert_offsets, p.n_experts, p.n_rows, p.num_n_tiles, BM, p.status, prefix,
+                                        reinterpret_cast<int32_t *>(smem + L::stage_c_off));
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
@@ -235,23 +308,32 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                     break;
                 }
                 const uint32_t fb = full_bar + 8 * stage;
-                const uint32_t a_dst = sbase + SmemLayout::a_off + stage * A_STAGE_BYTES;
-                const uint32_t b_dst = sbase + SmemLayout::b_off + stage * B_STAGE_BYTES;
+                const uint32_t a_dst = sbase + L::a_off + stage * A_STAGE_BYTES;
+                const uint32_t b_dst = sbase + L::b_off + stage * B_STAGE_BYTES;
+                const uint32_t sc_dst = scale_base + stage * SS::bytes;
                 if (skip) {
                     skip = false;  // withhold this load: consumers must time out
                 } else {
-                    // gathered rows arrive through the gather warps, not TMA
-                    uint32_t bytes = (gathered ? 0 : A_STAGE_BYTES) + B_STAGE_BYTES;
+                    // gathered rows (and their scales) arrive through the
+                    // gather warps, not TMA
+                    uint32_t bytes = (gathered ? 0 : A_STAGE_BYTES + 4 * SA_BOX) + B_STAGE_BYTES;
+                    if constexpr (MODE == WGRAD)
+                        bytes += 4 * BN;
                     bool second_half = true;
                     if constexpr (MODE == DGRAD) {
                         second_half = tl.n0 + 128 < p.N;
                         if (!second_half)
-                            bytes = A_STAGE_BYTES + B_STAGE_BYTES / 2;
+                            bytes -= B_STAGE_BYTES / 2;
                     }
                     if (lane == 0) {
                         mbar_arrive_expect_tx(fb, bytes);
                         filled_mask |= 1u << stage;
                         fill_parity = (fill_parity & ~(1u << stage)) | (phase << stage);
+                        if constexpr (!gathered)
+                            // the block's row scales: 132 from the 4-aligned row
+                            tma_load_2d(sc_dst, &tmSA, (int32_t)(tl.m0 & ~int64_t(3)), kb, fb);
+                        if constexpr (MODE == WGRAD)
+                            tma_load_2d(sc_dst + SS::b_off, &tmSB, (int32_t)tl.n0, kb, fb);
                     }
                     __syncwarp();
                     if constexpr (is_grouped(MODE)) {
@@ -312,8 +394,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                         break;
                     }
                     tc_fence_after();
-                    const uint32_t a_addr = sbase + SmemLayout::a_off + stage * A_STAGE_BYTES;
-                    const uint32_t b_addr = sbase + SmemLayout::b_off + stage * B_STAGE_BYTES;
+                    const uint32_t a_addr = sbase + L::a_off + stage * A_STAGE_BYTES;
+                    const uint32_t b_addr = sbase + L::b_off + stage * B_STAGE_BYTES;
                     const uint32_t d = tmem_base + buf * BN;
 #pragma unroll
                     for (int k = 0; k < BK / MMA_K; ++k) {
@@ -359,8 +441,12 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         const int quarter = warp & 3;        // TMEM lanes 32*quarter .. +31
         const int half = ew >> 2;            // output columns half*128 .. +127 of the tile
         const int row_in_tile = quarter * 32 + lane;
-        float *wscale = reinterpret_cast<float *>(smem + SmemLayout::stage_c_off + ew * STAGE_C_BYTES);
-        uint32_t buf = 0, tphase = 0;
+        // weight gradient: the block's 128 column scales of this warp's half,
+        // in the first 512 bytes of its epilogue staging block (idle until
+        // the tile's last block has been folded)
+        float *wscale = reinterpret_cast<float *>(smem + L::stage_c_off + ew * STAGE_C_BYTES);
+        uint32_t buf = 0, tphase = 0;        // TMEM partial buffer
+        uint32_t stage = 0, phase = 0;       // pipeline stage holding the block's scales
         bool ok = true;
         for (int64_t t = blockIdx.x; t < num_tiles && ok; t += gridDim.x) {
             const Tile tl = decode_tile<MODE>(t, p, prefix);
@@ -368,81 +454,54 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             const bool row_ok = row < tl.row_end;
             const int64_t col0 = tl.n0 + half * 128;
             const bool cols_ok = col0 < p.N;
-            int64_t arow = row;  // row of the scale array sA
-            if (gathered) {
-                int32_t v = row_ok ? p.row_index[row] : 0;
-                arow = (v < 0 || v >= p.n_tokens) ? 0 : v;
-            }
-            auto load_sa = [&](int kb) -> float { return row_ok ? __ldg(p.sA + (int64_t)kb * p.ld_sA + arow) : 0.0f; };
-            auto load_sb = [&](int kb) -> float {
-                if (!cols_ok)
-                    return 0.0f;
-                if constexpr (MODE == FPROP)
-                    return __ldg(p.sB + (col0 / 128) * p.ld_sB + kb);
-                else if constexpr (MODE == DGRAD)
-                    return __ldg(p.sB + (int64_t)kb * p.ld_sB + col0 / 128);
-                else if constexpr (is_grouped(MODE))
-                    return __ldg(p.sB + ((int64_t)tl.expert * (p.N / 128) + col0 / 128) * (p.K / 128) + kb);
-                else
-                    return 0.0f;
-            };
-            auto load_sbv = [&](int kb) -> float4 {
-                if (!cols_ok)
-                    return make_float4(0.f, 0.f, 0.f, 0.f);
-                return __ldg(reinterpret_cast<const float4 *>(p.sB + (int64_t)kb * p.ld_sB + col0) + lane);
-            };
+            // this thread's row scale inside a stage's slot (TMA boxes start
+            // at the 4-aligned row at or below the tile's first row)
+            const uint32_t sa_off = 4 * (uint32_t)((gathered ? 0 : (tl.m0 & 3)) + row_in_tile);
 
             // running FP32 sums of this thread's row, 128 columns as 64 pairs
             float2 acc[64];
 #pragma unroll
             for (int j = 0; j < 64; ++j)
                 acc[j] = make_float2(0.0f, 0.0f);
-            float sa_next = load_sa(0);
-            float sb_next = 0.0f;
-            float4 sbv_next = make_float4(0.f, 0.f, 0.f, 0.f);
-            if constexpr (MODE == WGRAD)
-                sbv_next = load_sbv(0);
-            else
-                sb_next = load_sb(0);
 
             for (int kb = 0; kb < num_kb; ++kb) {
-                const float sa = sa_next;
-                const float sb = sb_next;
-                const float4 sbv = sbv_next;
-                if (kb + 1 < num_kb) {
-                    sa_next = load_sa(kb + 1);
-                    if constexpr (MODE == WGRAD)
-                        sbv_next = load_sbv(kb + 1);
-                    else
-                        sb_next = load_sb(kb + 1);
+                // the stage's scales landed before its MMA was issued, so
+                // this wait only orders the reads after the copies
+                const uint8_t *slot = smem + L::scale_off + stage * SS::bytes;
+                bool got = mbar_wait(full_bar + 8 * stage, phase, wc, FP8FG_ETIMEOUT);
+                if (!__all_sync(0xffffffffu, got)) {
+                    ok = false;
+                    break;
                 }
-                if constexpr (MODE == WGRAD) {
-                    reinterpret_cast<float4 *>(wscale)[lane] = sbv;
-                    __syncwarp();
-                }
-                const bool got = mbar_wait(tfull_bar + 8 * buf, tphase, wc, FP8FG_ETIMEOUT);
+                float sa = *reinterpret_cast<const float *>(slot + sa_off);
+                if (gathered && !row_ok)
+                    sa = 0.0f;  // gathered slots of rows past the expert's end are not written
+                // B scales: the weight-block scale of this half, or (weight
+                // gradient) the half's 128 column scales, copied to the
+                // warp's own shared block for the fold
+                const float *bslot = reinterpret_cast<const float *>(slot + SS::b_off);
+                const float sb = MODE == WGRAD ? 0.0f : bslot[half];
+                if constexpr (MODE == WGRAD)
+                    reinterpret_cast<float4 *>(wscale)[lane] = reinterpret_cast<const float4 *>(bslot + half * 128)[lane];
+                // the stage's scales are read: its slot may be refilled
+                __syncwarp();
+                if (lane == 0)
+                    mbar_arrive(empty_bar + 8 * stage);
+                got = mbar_wait(tfull_bar + 8 * buf, tphase, wc, FP8FG_ETIMEOUT);
                 if (!__all_sync(0xffffffffu, got)) {
                     ok = false;
                     break;
                 }
                 tc_fence_after();
                 const uint32_t taddr = tmem_base + ((uint32_t)(quarter * 32) << 16) + buf * BN + half * 128;
-                const float s = sa * sb;
-                const float2 s2 = make_float2(s, s);
+                const float sab = sa * sb;
+                const float2 s2 = make_float2(sab, sab);
                 const float2 sa2 = make_float2(sa, sa);
-                // two loads in flight: chunk c+1 streams from TMEM while chunk
-                // c is folded in with paired FP32 FMAs
-                uint32_t r[2][CHUNK];
-                tmem_ld_chunk(taddr, r[0]);
-                tmem_wait_ld_chunk(r[0]);
-#pragma unroll
-                for (int c = 0; c < 128 / CHUNK; ++c) {
-                    if (c + 1 < 128 / CHUNK)
-                        tmem_ld_chunk(taddr + (c + 1) * CHUNK, r[(c + 1) & 1]);
+                // fold one 16-column chunk c (held in r) into the sums
+                auto fold = [&](int c, const uint32_t(&r)[CHUNK]) {
 #pragma unroll
                     for (int j = 0; j < CHUNK / 2; ++j) {
-                        const float2 pv =
-                            make_float2(__uint_as_float(r[c & 1][2 * j]), __uint_as_float(r[c & 1][2 * j + 1]));
+                        const float2 pv = make_float2(__uint_as_float(r[2 * j]), __uint_as_float(r[2 * j + 1]));
                         const int a = c * (CHUNK / 2) + j;
                         if constexpr (MODE == WGRAD) {
                             const float2 sc = reinterpret_cast<const float2 *>(wscale)[a];
@@ -451,16 +510,46 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                             acc[a] = __ffma2_rn(pv, s2, acc[a]);
                         }
                     }
-                    if (c + 1 < 128 / CHUNK)
-                        tmem_wait_ld_chunk(r[(c + 1) & 1]);
+                };
+                // The partial buffer is released as soon as all of its
+                // columns sit in registers: chunks 0..3 are loaded, then
+                // each is folded in while the load of chunk 4..7 takes its
+                // registers; once those four loads land the buffer goes back
+                // to the MMA and chunks 4..7 are folded after the release,
+                // off the MMA's critical path.
+                constexpr int HELD = 4;  // chunks in registers at a time
+                static_assert(HELD * 2 * CHUNK == 128, "two rounds of HELD chunks cover the half");
+                uint32_t r[HELD][CHUNK];
+#pragma unroll
+                for (int c = 0; c < HELD; ++c)
+                    tmem_ld_chunk(taddr + c * CHUNK, r[c]);
+#pragma unroll
+                for (int c = 0; c < HELD; ++c)
+                    tmem_wait_ld_chunk(r[c]);  // one wait; each call ties its registers to it
+#pragma unroll
+                for (int c = 0; c < HELD; ++c) {
+                    fold(c, r[c]);
+                    tmem_ld_chunk(taddr + (HELD + c) * CHUNK, r[c]);
                 }
+#pragma unroll
+                for (int c = 0; c < HELD; ++c)
+                    tmem_wait_ld_chunk(r[c]);
                 tc_fence_before();
                 __syncwarp();
                 if (lane == 0)
                     mbar_arrive(tempty_bar + 8 * buf);
+#pragma unroll
+                for (int c = 0; c < HELD; ++c)
+                    fold(HELD + c, r[c]);
+                if constexpr (MODE == WGRAD)
+                    __syncwarp();  // the column scales are read before the next block overwrites them
                 if (++buf == 2) {
                     buf = 0;
                     tphase ^= 1;
+                }
+                if (++stage == STAGES) {
+                    stage = 0;
+                    phase ^= 1;
                 }
             }
             if (!ok)
@@ -492,7 +581,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             {
                 constexpr int CW = OUT == OUT_BF16 ? 32 : (OUT == OUT_F32 ? 16 : 64);  // columns per 64-byte piece
                 constexpr int ESZ = OUT == OUT_BF16 ? 2 : (OUT == OUT_F32 ? 4 : 1);
-                uint8_t *const stg = smem + SmemLayout::stage_c_off + ew * STAGE_C_BYTES;
+                uint8_t *const stg = smem + L::stage_c_off + ew * STAGE_C_BYTES;
                 // write side: this lane's row, pieces swizzled by (lane / 2) % 4
                 uint8_t *const w_row = stg + lane * 64;
                 const int w_sw = (lane >> 1) & 3;
@@ -563,7 +652,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         setmaxnreg_dec<Regs<MODE>::LOW>();
         const int wrow = (warp - 2) * 64;          // first tile row of this warp
         const int chunk = lane & 7;                // 16-byte chunk of the row
-        int32_t *tok = reinterpret_cast<int32_t *>(smem + SmemLayout::tok_off);
+        int32_t *tok = reinterpret_cast<int32_t *>(smem + L::tok_off);
         uint32_t stage = 0, phase = 0;
         int64_t issued = 0, arrived = 0;          // blocks issued / blocks signalled
         uint32_t arrive_stage = 0;
@@ -602,7 +691,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                     ok = false;
                     break;
                 }
-                const uint32_t a_dst = sbase + SmemLayout::a_off + stage * A_STAGE_BYTES;
+                const uint32_t a_dst = sbase + L::a_off + stage * A_STAGE_BYTES;
                 const uint8_t *a_src = p.A + (int64_t)kb * BK + chunk * 16;
 #pragma unroll
                 for (int i = 0; i < 16; ++i) {
@@ -610,6 +699,17 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                     if (rr < nvalid)
                         cp_async16(a_dst + rr * 128 + ((chunk ^ (rr & 7)) << 4), a_src + (int64_t)tok[rr] * p.K);
                 }
+                // the rows' scales of this block, into the stage's scale slot,
+                // and (warp 2) the tile's two weight-block scales
+                const uint32_t sa_dst = scale_base + stage * SS::bytes;
+#pragma unroll
+                for (int j = 0; j < 2; ++j) {
+                    const int rr = wrow + 32 * j + lane;
+                    if (rr < nvalid)
+                        cp_async4(sa_dst + 4 * rr, p.sA + (int64_t)kb * p.ld_sA + tok[rr]);
+                }
+                if (warp == 2 && lane < 2 && tl.n0 + 128 * lane < p.N)
+                    cp_async4(sa_dst + SS::b_off + 4 * lane, weight_scale<MODE>(p, tl, kb, lane));
                 cp_async_commit();
                 ++issued;
                 cp_async_wait<2>();  // all but the two newest blocks have landed
@@ -625,8 +725,43 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         cp_async_wait<0>();
         while (arrived < issued)
             signal_oldest();
+    } else if (warp == 2 && MODE != WGRAD) {
+        // ------------------------------------------ weight-block scales ----
+        // The tile's two 128x128 weight-block scales of each contraction
+        // block, copied into the stage's scale slot with 4-byte cp.async;
+        // their completion is one arrival on the stage's "full" barrier.
+        setmaxnreg_dec<Regs<MODE>::LOW>();
+        uint32_t stage = 0, phase = 0;
+        bool ok = true;
+        for (int64_t t = blockIdx.x; t < num_tiles && ok; t += gridDim.x) {
+            const Tile tl = decode_tile<MODE>(t, p, prefix);
+            const bool two = tl.n0 + 128 < p.N;
+            for (int kb = 0; kb < num_kb; ++kb) {
+                bool got = true;
+                if (lane == 0)
+                    got = mbar_wait(empty_bar + 8 * stage, phase ^ 1, wc, FP8FG_ETIMEOUT);
+                got = __shfl_sync(0xffffffffu, got ? 1 : 0, 0) != 0;
+                if (!got) {
+                    ok = false;
+                    break;
+                }
+                if (lane == 0) {
+                    const uint32_t dst = scale_base + stage * SS::bytes + SS::b_off;
+                    cp_async4(dst, weight_scale<MODE>(p, tl, kb, 0));
+                    if (two)
+                        cp_async4(dst + 4, weight_scale<MODE>(p, tl, kb, 1));
+                    cp_async_mbar_arrive_noinc(full_bar + 8 * stage);
+                }
+                if (++stage == STAGES) {
+                    stage = 0;
+                    phase ^= 1;
+                }
+            }
+        }
+        // every copy into shared memory lands before the CTA can exit
+        asm volatile("cp.async.wait_all;" ::: "memory");
     } else {
-        // warps 2..3 complete warpgroup 0 and have no role
+        // warps 2..3 complete warpgroup 0; no role here
         setmaxnreg_dec<Regs<MODE>::LOW>();
     }
 
@@ -640,11 +775,17 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 
 // ------------------------------------------------------------ host side ----
 
+// Tensor maps of one launch: operands A and B, and the scale rows read by
+// TMA (A's row scales; the weight gradient's column scales).
+struct Maps {
+    CUtensorMap a, b, sa, sb;
+};
+
 template <int MODE, int OUT>
-int launch(const CUtensorMap &ta, const CUtensorMap &tb, const Params &p, int grid, cudaStream_t s)
+int launch(const Maps &m, const Params &p, int grid, cudaStream_t s)
 {
     auto k = gemm_kernel<MODE, OUT>;
-    if (cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)SmemLayout::total) !=
+    if (cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)SmemLayout<MODE>::total) !=
         cudaSuccess) {
         cudaGetLastError();
         return FP8FG_ECUDA;
@@ -658,14 +799,14 @@ int launch(const CUtensorMap &ta, const CUtensorMap &tb, const Params &p, int gr
     }
     if (fa.numRegs < Regs<MODE>::LAUNCH_MIN)
         return FP8FG_EUNSUPPORTED;
-    k<<<grid, NUM_THREADS, SmemLayout::total, s>>>(ta, tb, p);
+    k<<<grid, NUM_THREADS, SmemLayout<MODE>::total, s>>>(m.a, m.b, m.sa, m.sb, p);
     return launch_status();
 }
 
 template <int MODE>
-int launch_out(int out, const CUtensorMap &ta, const CUtensorMap &tb, const Params &p, int grid, cudaStream_t s)
+int launch_out(int out, const Maps &m, const Params &p, int grid, cudaStream_t s)
 {
-    return out == FP8FG_OUT_BF16 ? launch<MODE, OUT_BF16>(ta, tb, p, grid, s) : launch<MODE, OUT_F32>(ta, tb, p, grid, s);
+    return out == FP8FG_OUT_BF16 ? launch<MODE, OUT_BF16>(m, p, grid, s) : launch<MODE, OUT_F32>(m, p, grid, s);
 }
 
 bool fill_runtime(Params &p)
@@ -736,27 +877,37 @@ int gemm_entry(int mode, const uint8_t *A, const float *sA, int64_t lda, int64_t
     if (!fill_runtime(p))
         return FP8FG_ECUDA;
 
-    CUtensorMap ta, tb;
-    if (!make_map(&ta, A, (uint64_t)K, (uint64_t)M, (uint64_t)lda, BK, BM))
+    Maps m;
+    if (!make_map(&m.a, A, (uint64_t)K, (uint64_t)M, (uint64_t)lda, BK, BM))
         return FP8FG_ECUDA;
     bool okb;
     if (mode == DGRAD)  // weight [K][N], N contiguous: boxes of 128 N x 128 K
-        okb = make_map(&tb, B, (uint64_t)N, (uint64_t)K, (uint64_t)ldb, 128, BK);
+        okb = make_map(&m.b, B, (uint64_t)N, (uint64_t)K, (uint64_t)ldb, 128, BK);
     else
-        okb = make_map(&tb, B, (uint64_t)K, (uint64_t)N, (uint64_t)ldb, BK, BN);
+        okb = make_map(&m.b, B, (uint64_t)K, (uint64_t)N, (uint64_t)ldb, BK, BN);
     if (!okb)
         return FP8FG_ECUDA;
+    // row scales [K/128][ld_sA]: one box of SA_BOX per block; the weight
+    // gradient's column scales [K/128][ld_sB]: one box of BN per block
+    if (!make_map_f32_row(&m.sa, sA, (uint64_t)M, (uint64_t)(K / BK), (uint64_t)ld_sA, SA_BOX))
+        return FP8FG_ECUDA;
+    if (mode == WGRAD) {
+        if (!make_map_f32_row(&m.sb, sB, (uint64_t)N, (uint64_t)(K / BK), (uint64_t)ld_sB, BN))
+            return FP8FG_ECUDA;
+    } else {
+        m.sb = m.sa;  // unused
+    }
 
     const int64_t tiles = p.num_m_tiles * p.num_n_tiles;
     const int sms = sm_count();
     const int grid = (int)(tiles < sms ? tiles : sms);
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     if (out == OUT_E4M3)
-        return mode == FPROP ? launch<FPROP, OUT_E4M3>(ta, tb, p, grid, s) : launch<DGRAD, OUT_E4M3>(ta, tb, p, grid, s);
+        return mode == FPROP ? launch<FPROP, OUT_E4M3>(m, p, grid, s) : launch<DGRAD, OUT_E4M3>(m, p, grid, s);
     switch (mode) {
-    case FPROP: return launch_out<FPROP>(out, ta, tb, p, grid, s);
-    case DGRAD: return launch_out<DGRAD>(out, ta, tb, p, grid, s);
-    default: return launch_out<WGRAD>(out, ta, tb, p, grid, s);
+    case FPROP: return launch_out<FPROP>(out, m, p, grid, s);
+    case DGRAD: return launch_out<DGRAD>(out, m, p, grid, s);
+    default: return launch_out<WGRAD>(out, m, p, grid, s);
     }
 }
 
@@ -796,6 +947,11 @@ extern "C" int fp8_grouped_gemm(const uint8_t *Xq, const float *sX, int64_t ld_s
         return FP8FG_EINVAL;
     if (n_tokens >= (1ll << 31) || n_rows >= (1ll << 31) || K >= (1ll << 31) ||
         (int64_t)n_experts * N >= (1ll << 31))
+        return FP8FG_EINVAL;
+    // the kernels keep the experts' tile prefix in int32: reject any call
+    // whose largest possible tile count (every expert ending in a partial
+    // row tile) would not fit
+    if (((n_rows + (int64_t)n_experts * (BM - 1)) / BM) * ((N + BN - 1) / BN) >= (1ll << 31))
         return FP8FG_EINVAL;
     const int64_t esz = out == FP8FG_OUT_BF16 ? 2 : 4;
     if (ld_sX < n_tokens || ldy < N)
@@ -837,16 +993,20 @@ extern "C" int fp8_grouped_gemm(const uint8_t *Xq, const float *sX, int64_t ld_s
         return FP8FG_ECUDA;
     p.skip_first_load = 0;
 
-    CUtensorMap ta, tb;
+    Maps m;
     p.A = Xq;
-    // with a row index the A rows are gathered with cp.async (the A map is
-    // then unused but kept valid); without one, TMA loads 128-row A tiles
-    if (!make_map(&ta, Xq, (uint64_t)K, (uint64_t)n_tokens, (uint64_t)K, BK, row_index ? 1 : BM))
+    // with a row index the A rows and their scales are gathered with
+    // cp.async (the A and row-scale maps are then unused but kept valid);
+    // without one, TMA loads 128-row A tiles and their row scales
+    if (!make_map(&m.a, Xq, (uint64_t)K, (uint64_t)n_tokens, (uint64_t)K, BK, row_index ? 1 : BM))
         return FP8FG_ECUDA;
-    if (!make_map(&tb, Wq, (uint64_t)K, (uint64_t)n_experts * (uint64_t)N, (uint64_t)K, BK, BN))
+    if (!make_map(&m.b, Wq, (uint64_t)K, (uint64_t)n_experts * (uint64_t)N, (uint64_t)K, BK, BN))
         return FP8FG_ECUDA;
+    if (!make_map_f32_row(&m.sa, sX, (uint64_t)n_tokens, (uint64_t)(K / BK), (uint64_t)ld_sX, SA_BOX))
+        return FP8FG_ECUDA;
+    m.sb = m.sa;  // unused
     const int grid = sm_count();
     if (row_index)
-        return launch_out<GROUPED>(out, ta, tb, p, grid > 0 ? grid : 1, static_cast<cudaStream_t>(stream));
-    return launch_out<GROUPED_C>(out, ta, tb, p, grid > 0 ? grid : 1, static_cast<cudaStream_t>(stream));
+        return launch_out<GROUPED>(out, m, p, grid > 0 ? grid : 1, static_cast<cudaStream_t>(stream));
+    return launch_out<GROUPED_C>(out, m, p, grid > 0 ? grid : 1, static_cast<cudaStream_t>(stream));
 }

@@ -184,7 +184,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         tmem_relinquish();
     }
     if constexpr (MODE == GROUPED_C)
-        build_group_prefix<NUM_THREADS>(p.expert_offsets, p.n_experts, p.n_rows, p.num_n_tiles, BM, p.status, prefix);
+        build_group_prefix<NUM_THREADS>(p.expert_offsets, p.n_experts, p.n_rows, p.num_n_tiles, BM, p.status, prefix,
+                                        reinterpret_cast<int32_t *>(smem + SmemLayout::stage_c_off));
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
@@ -645,6 +646,11 @@ extern "C" int fp8_grouped_gemm_mx(const uint8_t *Xq, const float *sX, int64_t l
     if (n_experts < 1 || n_experts > MAX_EXPERTS)
         return FP8FG_EINVAL;
     if (n_rows >= (1ll << 31) || K >= (1ll << 31) || (int64_t)n_experts * N >= (1ll << 31))
+        return FP8FG_EINVAL;
+    // the kernels keep the experts' tile prefix in int32: reject any call
+    // whose largest possible tile count (every expert ending in a partial
+    // row tile) would not fit
+    if (((n_rows + (int64_t)n_experts * (BM - 1)) / BM) * ((N + BN - 1) / BN) >= (1ll << 31))
         return FP8FG_EINVAL;
     const int64_t esz = out == FP8FG_OUT_BF16 ? 2 : 4;
     if (ld_sX < n_rows || ldy < N || !expert_offsets)

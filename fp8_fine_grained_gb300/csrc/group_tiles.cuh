@@ -20,12 +20,14 @@ struct GroupTile {
 
 // Block-wide exclusive prefix over experts of (m-tiles x n-tiles) into
 // prefix[0..E] (prefix[E] = total tiles); malformed offsets are reported as
-// FP8FG_EDEVICE and clamped. All NT threads of the block call it.
+// FP8FG_EDEVICE and clamped. All NT threads of the block call it;
+// warp_sums is NT/32 ints of shared scratch (the kernels lend a region
+// that is idle during their prologue, so they declare no static shared
+// memory that would push their aligned dynamic region).
 template <int NT>
 __device__ void build_group_prefix(const int32_t *offsets, int E, int64_t n_rows, int64_t n_tiles_n, int bm,
-                                   int *status, int32_t *prefix)
+                                   int *status, int32_t *prefix, int32_t *warp_sums)
 {
-    __shared__ int32_t warp_sums[NT / 32];
     const int per = (E + NT - 1) / NT;
     const int e0 = threadIdx.x * per;
     int32_t local[16];  // per <= 4096 / NT + 1

@@ -169,6 +169,21 @@ __device__ __forceinline__ void cp_async16_hint(uint32_t dst, const void *src, u
                  : "memory");
 }
 
+// 4-byte global -> shared copy (cached in L1 and L2; .ca is the only form
+// of cp.async that copies fewer than 16 bytes).
+__device__ __forceinline__ void cp_async4(uint32_t dst, const void *src)
+{
+    asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(dst), "l"(src) : "memory");
+}
+
+// Arrive once on `bar` when every cp.async this thread has issued so far
+// has completed. The arrival is not pre-counted (.noinc): the barrier's
+// expected arrival count must include it.
+__device__ __forceinline__ void cp_async_mbar_arrive_noinc(uint32_t bar)
+{
+    asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(bar) : "memory");
+}
+
 __device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
 
 // Wait until at most N of this thread's committed groups are still in flight.

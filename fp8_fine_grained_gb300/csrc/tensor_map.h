@@ -46,4 +46,22 @@ inline bool make_map(CUtensorMap *m, const void *base, uint64_t cols, uint64_t r
               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// 2-D FP32 tensor [rows][cols] with row pitch `ld` elements; box
+// box_cols x 1 (one row of scales per copy), no swizzle. Out-of-range box
+// elements read 0.
+inline bool make_map_f32_row(CUtensorMap *m, const void *base, uint64_t cols, uint64_t rows, uint64_t ld,
+                             uint32_t box_cols)
+{
+    EncodeTiledFn fn = encode_fn();
+    if (!fn)
+        return false;
+    cuuint64_t dims[2] = {cols, rows};
+    cuuint64_t strides[1] = {ld * 4};
+    cuuint32_t box[2] = {box_cols, 1};
+    cuuint32_t estr[2] = {1, 1};
+    return fn(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, const_cast<void *>(base), dims, strides, box, estr,
+              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_NONE,
+              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 }  // namespace fp8fg

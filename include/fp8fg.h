@@ -31,6 +31,11 @@
  *             sA(i,kb) * sB(j,kb) * P(i,j,kb), P the block's FP8 x FP8 dot
  *             product from the tensor cores (FP32 in tensor memory), the sum
  *             over kb kept in FP32 registers.
+ *   inputs    bf16 inputs must be finite. A NaN or an infinity in a group is
+ *             outside the contract: the call still returns, no kernel hangs
+ *             or touches memory outside its arguments, but that group's
+ *             codes and scale (and every GEMM output that reads them) are
+ *             unspecified. The pages give no rule for non-finite values.
  *
  * Conventions for every call:
  *   - All pointers are DEVICE pointers owned by the caller. The library
@@ -283,7 +288,9 @@ FP8FG_API int fp8_gemm_blockscaled_e4m3(int mode,
  *             not written.
  *   Wq        E4M3 [n_experts][N][K]; sW FP32 [n_experts][N/128][K/128].
  *   Y         [n_rows][ldy], FP32 or bf16 per `out`.
- *   K % 128 == 0, N % 128 == 0, 1 <= n_experts <= 4096.
+ *   K % 128 == 0, N % 128 == 0, 1 <= n_experts <= 4096, and the largest
+ *   possible tile count ((n_rows + 127 n_experts) / 128) x ceil(N / 256)
+ *   below 2^31 (else EINVAL).
  *   Alignment: Xq, Wq, sX, Y 16-byte aligned; K % 16 == 0; ld_sX % 4 == 0;
  *   ldy*sizeof(out) % 16 == 0.
  * ------------------------------------------------------------------- */

@@ -10,24 +10,46 @@ import torch.multiprocessing as mp
 import bench
 
 
-def test_clock_summary_parses_nvidia_smi_csv(tmp_path):
-    p = tmp_path / "c.csv"
-    p.write_text("\n".join([
-        "2070, 2070, 900.5, 0x0, Not Active, Not Active, Not Active, Not Active",
-        "1950, 2070, 1390.0, 0x4, Not Active, Not Active, Not Active, Active",
-        "300, 2070, 200.0, 0x1, Not Active, Not Active, Not Active, Not Active",   # idle sample
+def _clock_lines():
+    return "\n".join([
+        "2026/12/02 10:00:00.000, 1995, 2070, 180.0, 0x0, Not Active, Not Active, Not Active, Not Active",
+        "2026/12/02 10:00:00.050, 2070, 2070, 900.5, 0x0, Not Active, Not Active, Not Active, Not Active",
+        "2026/12/02 10:00:00.100, 1950, 2070, 1390.0, 0x4, Not Active, Not Active, Not Active, Active",
+        "2026/12/02 10:00:00.150, 1995, 2070, 200.0, 0x0, Not Active, Not Active, Not Active, Not Active",
         "garbage line",
-    ]))
-    s = bench.summarize_clocks(str(p))
-    assert s["samples"] == 3
+    ])
+
+
+def test_clock_summary_keeps_only_samples_inside_the_timed_region(tmp_path):
+    p = tmp_path / "c.csv"
+    p.write_text(_clock_lines())
+    t = bench._stamp("2026/12/02 10:00:00.000")
+    s = bench.summarize_clocks(str(p), [(t + 0.04, t + 0.11)])
+    assert s["samples"] == 2              # the idle samples before and after are left out
     assert s["sm_max_mhz"] == 2070
-    assert s["sm_mhz"] == 2010.0          # median of the two loaded samples
+    assert s["sm_mhz"] == 2010.0          # median of the two samples inside
     assert s["reasons"] == ["sw_power_cap"]
 
 
+def test_clock_summary_says_so_when_no_sample_is_inside(tmp_path):
+    p = tmp_path / "c.csv"
+    p.write_text(_clock_lines())
+    t = bench._stamp("2026/12/02 10:00:00.000")
+    s = bench.summarize_clocks(str(p), [(t + 0.06, t + 0.08)])   # 20 ms, between two samples
+    assert s["samples"] == 0 and s["sm_mhz"] is None and "no nvidia-smi sample" in s["note"]
+    assert s["within_0.25s_of_timed_region"]["samples"] == 4
+
+
 def test_clock_summary_without_samples(tmp_path):
-    s = bench.summarize_clocks(str(tmp_path / "missing.csv"))
+    s = bench.summarize_clocks(str(tmp_path / "missing.csv"), [(0.0, 1.0)])
     assert s["samples"] == 0 and s["reasons"] == ["unsampled"]
+
+
+def test_both_arms_print_the_same_config():
+    for w in bench.WORKLOADS:
+        assert bench.config_of(w, 1) == bench.config_of(w, 1)
+    src = open(bench.__file__).read()
+    assert src.count('"config": config_of(args.workload, world)') == 2
 
 
 def test_traffic_lookup_follows_kernel_sources(tmp_path, monkeypatch):
