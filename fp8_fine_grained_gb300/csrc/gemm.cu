@@ -16,25 +16,27 @@
 //               dequantisation scales travel in the same stage: the tile's
 //               128 row scales (and, for the weight gradient, its 256 column
 //               scales) by TMA, the two 128x128 weight-block scales by 4-byte
-//               cp.async, so the promotion warps read them from shared memory
-//               instead of waiting on L2 once per block.
-//   warp 1      MMA issuer: allocates all 512 tensor-memory columns, issues
-//               4 x tcgen05.mma (M128 N256 K32, E4M3 -> FP32) per block into
-//               one of two 256-column TMEM partial buffers, and commits to
-//               the stage's "empty" and the buffer's "full" barrier.
-//   warps 2..3  MoE experts with a row index: gather the tile's token rows
-//               into the A stage with cp.async; otherwise no role (they
-//               complete warpgroup 0 so that setmaxnreg can move its
-//               registers to the promotion warpgroups).
+//               cp.async from the producer, so the promotion warps read them
+//               from shared memory instead of waiting on L2 once per block.
+//   warps 1..3  MMA issuers: warp 1 allocates all 512 tensor-memory
+//               columns; per contraction block one of them (in turn) issues
+//               4 x tcgen05.mma (M128 N256 K32, E4M3 -> FP32) into one of two
+//               256-column TMEM partial buffers and commits to the buffer's
+//               "full" barrier (the promotion warps free the stage once they
+//               have seen that commit). Three issuers spread the issue cost
+//               over three SMSPs. MoE rows gathered through a row index:
+//               warp 1 issues every block and warps 2..3 gather the tile's
+//               token rows and their scales into the stage with cp.async.
 //   warps 4..11 promotion/epilogue: each thread owns one output row and 128
 //               columns; per block it reads its scales from the stage, loads
-//               the partial from TMEM
-//               (tcgen05.ld 32x32b, 32 columns at a time, two loads in
-//               flight), does acc = fma(P, sA*sB, acc) in FP32 registers
-//               (paired FP32 FMAs) and frees the TMEM buffer, so the MMA of
-//               block kb+1 overlaps the promotion of block kb. After the
-//               last block it rounds its rows and stores them through a
-//               shared-memory staging block, 8 rows x 64 bytes per store.
+//               the partial from TMEM (tcgen05.ld 32x32b, 16 columns per
+//               load), releases the buffer once all 128 columns are in
+//               registers, and does acc = fma(P, sA*sB, acc) in FP32
+//               registers (paired FP32 FMAs), half before the release and
+//               half after it, so the MMA of block kb+2 overlaps the end of
+//               the promotion of block kb. After the last block it rounds
+//               its rows and stores them through a shared-memory staging
+//               block, 8 rows x 64 bytes per store.
 // Every wait is bounded (global timer); a wait that runs out records
 // FP8FG_ETIMEOUT in the device status word and all roles leave their loops,
 // drain their own in-flight copies and MMAs, and release tensor memory.
@@ -141,8 +143,8 @@ template <int MODE> struct SmemLayout {
     static constexpr uint32_t full_off = bar_off;
     static constexpr uint32_t empty_off = full_off + 8 * STAGES;
     static constexpr uint32_t tfull_off = empty_off + 8 * STAGES;
-    static constexpr uint32_t tempty_off = tfull_off + 8 * 2;
-    static constexpr uint32_t tmem_ptr_off = tempty_off + 8 * 2;
+    static constexpr uint32_t tempty_off = tfull_off + 8 * 2;          // one per stage (block g: g % STAGES)
+    static constexpr uint32_t tmem_ptr_off = tempty_off + 8 * STAGES;
     static constexpr uint32_t abort_off = tmem_ptr_off + 4;
     static constexpr uint32_t misc_end = abort_off + 4;
     // per promotion warp: epilogue staging block
@@ -162,10 +164,14 @@ static_assert(SmemLayout<GROUPED>::total <= 232448, "shared memory budget");
 static_assert(SmemLayout<GROUPED_C>::total <= 232448, "shared memory budget");
 
 // Arrivals that complete a stage's "full" barrier: the producer's
-// arrive.expect_tx; the completion of warp 2's 4-byte weight-scale copies
+// arrive.expect_tx; the completion of its 4-byte weight-scale copies
 // (fprop, dgrad, experts with rows in expert order; the weight gradient's
 // scales all come by TMA); or, for MoE rows gathered through a row index,
 // the two gather warps (whose copies include the weight-block scales).
+// Threads issuing MMAs: warps 1..3 take the blocks in turn, except for MoE
+// rows gathered through a row index, where warps 2 and 3 gather A rows.
+template <int MODE> constexpr int MMA_ISSUERS() { return MODE == GROUPED ? 1 : 3; }
+
 template <int MODE> constexpr uint32_t full_arrivals()
 {
     return MODE == GROUPED ? 1 + GATHER_WARPS : (MODE == WGRAD ? 1 : 2);
@@ -255,15 +261,20 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     if (threadIdx.x == 0) {
         for (int s = 0; s < STAGES; ++s) {
             mbar_init(full_bar + 8 * s, full_arrivals<MODE>());
-            // freed by the MMA's commit and by every promotion warp once it
-            // has read the stage's scales (before it waits for the block's
-            // partial, so refills are not held back by the fold)
-            mbar_init(empty_bar + 8 * s, 1 + EPI_WARPS);
+            // freed by the promotion warps: each arrives once it has read
+            // the stage's scales and seen the block's MMAs complete (which
+            // covers the tensor cores' reads of the stage), so the MMA
+            // issuer needs no commit of its own for the stage
+            mbar_init(empty_bar + 8 * s, EPI_WARPS);
         }
-        for (int b = 0; b < 2; ++b) {
+        for (int b = 0; b < 2; ++b)
             mbar_init(tfull_bar + 8 * b, 1);
-            mbar_init(tempty_bar + 8 * b, EPI_WARPS);
-        }
+        // "partial read" barriers, one per stage rather than per TMEM buffer:
+        // an issuer may be a few blocks ahead of the others, and with one
+        // barrier per buffer it could test a phase two behind the one it
+        // needs, which a parity wait cannot tell apart
+        for (int s = 0; s < STAGES; ++s)
+            mbar_init(tempty_bar + 8 * s, EPI_WARPS);
         *abort_flag = 0;
         fence_mbar_init();
         tma_prefetch_desc(&tmA);
@@ -332,8 +343,16 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                         if constexpr (!gathered)
                             // the block's row scales: 132 from the 4-aligned row
                             tma_load_2d(sc_dst, &tmSA, (int32_t)(tl.m0 & ~int64_t(3)), kb, fb);
-                        if constexpr (MODE == WGRAD)
+                        if constexpr (MODE == WGRAD) {
                             tma_load_2d(sc_dst + SS::b_off, &tmSB, (int32_t)tl.n0, kb, fb);
+                        } else if constexpr (!gathered) {
+                            // the weight-block scales of the tile's two column
+                            // halves (4-byte copies: one FP32 per block and half)
+                            cp_async4(sc_dst + SS::b_off, weight_scale<MODE>(p, tl, kb, 0));
+                            if (tl.n0 + 128 < p.N)
+                                cp_async4(sc_dst + SS::b_off + 4, weight_scale<MODE>(p, tl, kb, 1));
+                            cp_async_mbar_arrive_noinc(fb);
+                        }
                     }
                     __syncwarp();
                     if constexpr (is_grouped(MODE)) {
@@ -361,6 +380,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 }
             }
         }
+        // the weight-scale copies of the last stages land before the CTA exits
+        asm volatile("cp.async.wait_all;" ::: "memory");
         if (!ok && lane == 0) {
             // drain: every issued fill must land before the CTA exits
             WaitCtl drain{abort_flag, p.status, p.wait_limit_ns};
@@ -373,20 +394,39 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 }
             }
         }
-    } else if (warp == 1) {
+    } else if (warp >= 1 && warp <= MMA_ISSUERS<MODE>()) {
         // ---------------------------------------------------------- MMA ----
+        // Issuing a block's four MMAs and its commit keeps the issuing
+        // warp's SMSP busy for about 400 cycles, time the promotion warps on
+        // that SMSP (bound to its TMEM lane quarter) lose. The blocks are
+        // dealt round-robin to three issuers on three SMSPs (warps 1, 2, 3):
+        // MMAs of different blocks are independent (each block starts with
+        // accumulate off), and each issuer's commits track its own MMAs.
         setmaxnreg_dec<Regs<MODE>::LOW>();
         if (lane == 0) {
             constexpr uint32_t IDESC = idesc_e4m3_f32(BM, BN, MODE == DGRAD);
-            uint32_t stage = 0, phase = 0, buf = 0, tphase = 0;
+            constexpr int NI = MMA_ISSUERS<MODE>();
+            const int issuer = warp - 1;
             int committed = 0;
             uint32_t last_buf = 0, last_par = 0;
             bool ok = true;
+            int64_t g = 0;  // the CTA's block counter (tile-major)
             for (int64_t t = blockIdx.x; t < num_tiles && ok; t += gridDim.x) {
-                for (int kb = 0; kb < num_kb; ++kb) {
-                    if (!mbar_wait(tempty_bar + 8 * buf, tphase ^ 1, wc, FP8FG_ETIMEOUT)) {
-                        ok = false;
-                        break;
+                for (int kb = 0; kb < num_kb; ++kb, ++g) {
+                    if ((int)(g % NI) != issuer)
+                        continue;
+                    const uint32_t stage = (uint32_t)(g % STAGES), phase = (uint32_t)((g / STAGES) & 1);
+                    const uint32_t buf = (uint32_t)(g & 1), tphase = (uint32_t)((g >> 1) & 1);
+                    // the buffer is free once block g-2's partial has been
+                    // read out (its barrier: stage (g-2) % STAGES, that
+                    // block's phase); the first two blocks find it free
+                    if (g >= 2) {
+                        const int64_t h = g - 2;
+                        if (!mbar_wait(tempty_bar + 8 * (uint32_t)(h % STAGES), (uint32_t)((h / STAGES) & 1), wc,
+                                       FP8FG_ETIMEOUT)) {
+                            ok = false;
+                            break;
+                        }
                     }
                     tc_fence_after();
                     if (!mbar_wait(full_bar + 8 * stage, phase, wc, FP8FG_ETIMEOUT)) {
@@ -410,23 +450,14 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                             bdesc = smem_desc_sw128(b_addr + k * MMA_K, 0, 1024);
                         mma_f8f6f4(d, adesc, bdesc, IDESC, k > 0 ? 1u : 0u);
                     }
-                    mma_commit(empty_bar + 8 * stage);
                     mma_commit(tfull_bar + 8 * buf);
                     committed = 1;
                     last_buf = buf;
                     last_par = tphase;
-                    if (++stage == STAGES) {
-                        stage = 0;
-                        phase ^= 1;
-                    }
-                    if (++buf == 2) {
-                        buf = 0;
-                        tphase ^= 1;
-                    }
                 }
             }
             if (!ok && committed) {
-                // drain: the last commit covers every MMA issued before it
+                // drain: the last commit covers every MMA this thread issued before it
                 const uint32_t bar = tfull_bar + 8 * last_buf;
                 const uint64_t t0 = global_timer_ns();
                 while (!mbar_try_wait(bar, last_par) && global_timer_ns() - t0 < p.wait_limit_ns) {
@@ -483,15 +514,17 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 const float sb = MODE == WGRAD ? 0.0f : bslot[half];
                 if constexpr (MODE == WGRAD)
                     reinterpret_cast<float4 *>(wscale)[lane] = reinterpret_cast<const float4 *>(bslot + half * 128)[lane];
-                // the stage's scales are read: its slot may be refilled
-                __syncwarp();
-                if (lane == 0)
-                    mbar_arrive(empty_bar + 8 * stage);
                 got = mbar_wait(tfull_bar + 8 * buf, tphase, wc, FP8FG_ETIMEOUT);
                 if (!__all_sync(0xffffffffu, got)) {
                     ok = false;
                     break;
                 }
+                // the block's MMAs are complete and its scales read (the
+                // weight gradient's column scales copied): the stage may be
+                // refilled
+                __syncwarp();
+                if (lane == 0)
+                    mbar_arrive(empty_bar + 8 * stage);
                 tc_fence_after();
                 const uint32_t taddr = tmem_base + ((uint32_t)(quarter * 32) << 16) + buf * BN + half * 128;
                 const float sab = sa * sb;
@@ -537,7 +570,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 tc_fence_before();
                 __syncwarp();
                 if (lane == 0)
-                    mbar_arrive(tempty_bar + 8 * buf);
+                    mbar_arrive(tempty_bar + 8 * stage);
 #pragma unroll
                 for (int c = 0; c < HELD; ++c)
                     fold(HELD + c, r[c]);
@@ -725,43 +758,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         cp_async_wait<0>();
         while (arrived < issued)
             signal_oldest();
-    } else if (warp == 2 && MODE != WGRAD) {
-        // ------------------------------------------ weight-block scales ----
-        // The tile's two 128x128 weight-block scales of each contraction
-        // block, copied into the stage's scale slot with 4-byte cp.async;
-        // their completion is one arrival on the stage's "full" barrier.
-        setmaxnreg_dec<Regs<MODE>::LOW>();
-        uint32_t stage = 0, phase = 0;
-        bool ok = true;
-        for (int64_t t = blockIdx.x; t < num_tiles && ok; t += gridDim.x) {
-            const Tile tl = decode_tile<MODE>(t, p, prefix);
-            const bool two = tl.n0 + 128 < p.N;
-            for (int kb = 0; kb < num_kb; ++kb) {
-                bool got = true;
-                if (lane == 0)
-                    got = mbar_wait(empty_bar + 8 * stage, phase ^ 1, wc, FP8FG_ETIMEOUT);
-                got = __shfl_sync(0xffffffffu, got ? 1 : 0, 0) != 0;
-                if (!got) {
-                    ok = false;
-                    break;
-                }
-                if (lane == 0) {
-                    const uint32_t dst = scale_base + stage * SS::bytes + SS::b_off;
-                    cp_async4(dst, weight_scale<MODE>(p, tl, kb, 0));
-                    if (two)
-                        cp_async4(dst + 4, weight_scale<MODE>(p, tl, kb, 1));
-                    cp_async_mbar_arrive_noinc(full_bar + 8 * stage);
-                }
-                if (++stage == STAGES) {
-                    stage = 0;
-                    phase ^= 1;
-                }
-            }
-        }
-        // every copy into shared memory lands before the CTA can exit
-        asm volatile("cp.async.wait_all;" ::: "memory");
     } else {
-        // warps 2..3 complete warpgroup 0; no role here
+        // completes warpgroup 0 (warps 2..3 when warp 1 issues every block);
+        // no role here
         setmaxnreg_dec<Regs<MODE>::LOW>();
     }
 
