@@ -385,10 +385,14 @@ def load_traffic(workload):
 
 
 def time_parts(W, args, pg, clocks, stream, flush_l2):
-    """W untimed warm-up steps, then exactly K timed steps of the workload's
-    parts, each part between CUDA events on the launching stream, L2 flushed
-    before every step outside the events. Returns the mean ms of every part
-    (max over ranks) and the host bounds of the timed region."""
+    """W untimed warm-up steps, then exactly K timed steps of the workload
+    with one CUDA event pair around each whole step (the parts back to
+    back, as an application runs them: consecutive kernels may overlap
+    their launch and set-up), L2 flushed before every step outside the
+    events. Then K more steps with an event after every part, for the
+    per-kernel breakdown (events between kernels add about 2 us each and
+    stop that overlap). Returns the mean ms of every part and of the whole
+    step (max over ranks) and the host bounds of the first timed region."""
     import torch
 
     import fp8_fine_grained_gb300 as fg
@@ -403,27 +407,38 @@ def time_parts(W, args, pg, clocks, stream, flush_l2):
     torch.cuda.synchronize()
     if fg.device_status() != 0:
         raise RuntimeError("device status after warm-up")
-    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(n + 1)] for _ in range(args.steps)]
     if pg:
         pg.barrier()
     torch.cuda.synchronize()
+    whole = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(args.steps)]
     t0 = time.time()
     for i in range(args.steps):
         flush_l2()                           # outside the events
+        whole[i][0].record(stream)
+        for p_ in parts:
+            p_.fn()
+        whole[i][1].record(stream)
+    torch.cuda.synchronize()
+    t1 = time.time()
+    clocks.mark(t0, t1)
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(n + 1)] for _ in range(args.steps)]
+    for i in range(args.steps):
+        flush_l2()
         ev[i][0].record(stream)
         for j, p_ in enumerate(parts):
             p_.fn()
             ev[i][j + 1].record(stream)
     torch.cuda.synchronize()
-    t1 = time.time()
-    clocks.mark(t0, t1)
+    clocks.mark(t1, time.time())
     if pg:
         pg.barrier()
     if fg.device_status() != 0:
         raise RuntimeError("device status after timing")
+    step_ms = sum(whole[i][0].elapsed_time(whole[i][1]) for i in range(args.steps)) / args.steps
     part_ms = [sum(ev[i][j].elapsed_time(ev[i][j + 1]) for i in range(args.steps)) / args.steps
                for j in range(n)]
-    return reduce_max(part_ms, pg), (t0, t1)
+    vals = reduce_max(part_ms + [step_ms], pg)
+    return vals[:n], vals[n], (t0, t1)
 
 
 def kernel_entries(parts, part_ms, traffic, hbm, fp8_peak):
@@ -544,11 +559,10 @@ def run_ours(args):
     flops, dims = W["flops"], W["dims"]
     n = len(parts)
     with clocks:
-        part_ms, region = time_parts(W, args, pg, clocks, stream, flush_l2)
+        part_ms, ms_step, region = time_parts(W, args, pg, clocks, stream, flush_l2)
     clk = clocks.summary(region)
 
     e2e = e2e_run(W, args, dev, rank, fg, synth, pg) if args.workload in WORKLOADS else None
-    ms_step = sum(part_ms)
     value = world * flops / (ms_step * 1e-3) / 1e12
 
     # the other workloads of the measurement plan, each timed the same way
@@ -562,11 +576,12 @@ def run_ours(args):
             Wc = build(name, dev, rank, fg, synth)
             cclk = ClockSampler(local)
             with cclk:
-                cms, creg = time_parts(Wc, args, pg, cclk, stream, flush_l2)
+                cms, cstep, creg = time_parts(Wc, args, pg, cclk, stream, flush_l2)
             kern = kernel_entries(Wc["parts"], cms, load_traffic(name), hbm, fp8_peak)
             dom = max(range(len(cms)), key=lambda j: cms[j])
-            configs[name] = {"workload": WORKLOADS[name], "ms_per_step": round(sum(cms), 4),
-                             "value": round(world * Wc["flops"] / (sum(cms) * 1e-3) / 1e12, 2),
+            configs[name] = {"workload": WORKLOADS[name], "ms_per_step": round(cstep, 4),
+                             "sum_of_parts_ms": round(sum(cms), 4),
+                             "value": round(world * Wc["flops"] / (cstep * 1e-3) / 1e12, 2),
                              "unit": "TFLOP/s", "dims": Wc["dims"],
                              "roofline": {k: kern[dom][k] for k in ("kernel", "bound", "achieved", "peak", "unit",
                                                                     "frac", "traffic")},
@@ -601,6 +616,9 @@ def run_ours(args):
         "steps": args.steps,
         "warmup": args.warmup,
         "ms_per_step": round(ms_step, 4),
+        "timing": "value and ms_per_step: one CUDA event pair around each of the K whole steps; "
+                  "kernels: K further steps with an event after every part (sum_of_parts_ms)",
+        "sum_of_parts_ms": round(sum(part_ms), 4),
         "higher_is_better": True,
         "scaling": "weak",
         "vs_baseline": None,
@@ -613,6 +631,7 @@ def run_ours(args):
         "kernels": kernels,
         "clocks": clk,
         "gpu_launches": n * args.steps,
+        "gpu_launches_breakdown_pass": n * args.steps,
     }
     if e2e:
         line["e2e"] = {"value": round(world * flops / (e2e["ms"] * 1e-3) / 1e12, 2),
@@ -622,12 +641,52 @@ def run_ours(args):
                                    "(two buffer sets, three streams)"}
     if configs:
         line["configs"] = configs
+    if args.workload in ("dense", "dense_mx", "dense_e4m3"):
+        ref = cublas_fp8_reference(dev)
+        line["fp8_cublas_reference"] = ref
+        if ref.get("tflops"):
+            line["fp8_cublas_reference"]["gemm_vs_cublas"] = round(dk["achieved"] / ref["tflops"], 4)
     if not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(args.workload, budget_s=args.cpu_seconds)
     print(json.dumps(line), flush=True)
     if pg:
         pg.destroy_process_group()
     return line
+
+
+def cublas_fp8_reference(dev, M=4096, N=7168, K=7168, steps=20):
+    """Context for the FP8 peak: cuBLAS's per-tensor-scaled FP8 GEMM
+    (torch._scaled_mm, E4M3 x E4M3 -> bf16, no block scales and no
+    promotion) on the dense shape, TFLOP/s from CUDA events, L2 flushed
+    between calls. None where the call is unavailable."""
+    import torch
+    try:
+        g = torch.Generator(device=dev)
+        g.manual_seed(0)
+        a = torch.randn(M, K, generator=g, device=dev).to(torch.float8_e4m3fn)
+        b = torch.randn(N, K, generator=g, device=dev).to(torch.float8_e4m3fn).t()
+        one = torch.ones((), dtype=torch.float32, device=dev)
+        flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
+
+        def call():
+            return torch._scaled_mm(a, b, scale_a=one, scale_b=one, out_dtype=torch.bfloat16)
+        for _ in range(3):
+            call()
+        ts = []
+        for _ in range(steps):
+            flush.zero_()
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record()
+            call()
+            e1.record()
+            ts.append((e0, e1))
+        torch.cuda.synchronize()
+        ms = sum(x.elapsed_time(y) for x, y in ts) / steps
+        return {"tflops": round(2.0 * M * N * K / (ms * 1e-3) / 1e12, 1), "ms": round(ms, 4),
+                "what": "torch._scaled_mm (cuBLAS), per-tensor scales, %dx%dx%d, bf16 out; context only, "
+                        "not the roofline denominator" % (M, N, K)}
+    except Exception as e:  # the call is missing or unsupported on this build
+        return {"tflops": None, "why": type(e).__name__}
 
 
 def config_of(workload, world):

@@ -296,6 +296,11 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         tmem_alloc(sbase + L::tmem_ptr_off, TMEM_COLS);
         tmem_relinquish();
     }
+    // Everything above touches only this CTA's shared and tensor memory;
+    // inputs written by the previous kernel in the stream (for example the
+    // quantiser, which lets this grid launch under its last wave) are read
+    // only after this wait.
+    griddep_wait();
     if constexpr (is_grouped(MODE))
         build_group_prefix<NUM_THREADS>(p.expert_offsets, p.n_experts, p.n_rows, p.num_n_tiles, BM, p.status, prefix,
                                         reinterpret_cast<int32_t *>(smem + L::stage_c_off));
@@ -806,7 +811,23 @@ int launch(const Maps &m, const Params &p, int grid, cudaStream_t s)
     }
     if (fa.numRegs < Regs<MODE>::LAUNCH_MIN)
         return FP8FG_EUNSUPPORTED;
-    k<<<grid, NUM_THREADS, SmemLayout<MODE>::total, s>>>(m.a, m.b, m.sa, m.sb, p);
+    // programmatic stream serialization: the grid may launch while the
+    // previous kernel's last CTAs run; the kernel waits (griddep_wait)
+    // before it reads anything that kernel wrote
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)grid);
+    cfg.blockDim = dim3(NUM_THREADS);
+    cfg.dynamicSmemBytes = SmemLayout<MODE>::total;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    if (cudaLaunchKernelEx(&cfg, k, m.a, m.b, m.sa, m.sb, p) != cudaSuccess) {
+        cudaGetLastError();
+        return FP8FG_ECUDA;
+    }
     return launch_status();
 }
 

@@ -183,6 +183,11 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         tmem_alloc(sbase + SmemLayout::tmem_ptr_off, TMEM_COLS);
         tmem_relinquish();
     }
+    // Everything above touches only this CTA's shared and tensor memory;
+    // inputs written by the previous kernel in the stream (for example the
+    // quantiser, which lets this grid launch under its last wave) are read
+    // only after this wait.
+    griddep_wait();
     if constexpr (MODE == GROUPED_C)
         build_group_prefix<NUM_THREADS>(p.expert_offsets, p.n_experts, p.n_rows, p.num_n_tiles, BM, p.status, prefix,
                                         reinterpret_cast<int32_t *>(smem + SmemLayout::stage_c_off));
@@ -550,7 +555,23 @@ int launch(const CUtensorMap &ta, const CUtensorMap &tb, const Params &p, int gr
         cudaGetLastError();
         return FP8FG_ECUDA;
     }
-    k<<<grid, NUM_THREADS, SmemLayout::total, s>>>(ta, tb, p);
+    // programmatic stream serialization: the grid may launch while the
+    // previous kernel's last CTAs run; the kernel waits (griddep_wait)
+    // before it reads anything that kernel wrote
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)grid);
+    cfg.blockDim = dim3(NUM_THREADS);
+    cfg.dynamicSmemBytes = SmemLayout::total;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    if (cudaLaunchKernelEx(&cfg, k, ta, tb, p) != cudaSuccess) {
+        cudaGetLastError();
+        return FP8FG_ECUDA;
+    }
     return launch_status();
 }
 

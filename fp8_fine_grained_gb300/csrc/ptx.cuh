@@ -23,6 +23,21 @@ __device__ __forceinline__ uint64_t global_timer_ns()
 
 __device__ __forceinline__ uint32_t lane_id() { return threadIdx.x & 31u; }
 
+// ---------------------------------------------- programmatic dependency ----
+
+// Let the grid launched after this one in the stream with programmatic
+// stream serialization start launching: it launches once every CTA of this
+// grid has executed this (or exited), so the earliest point is when the
+// grid's last CTAs are running.
+__device__ __forceinline__ void griddep_launch_dependents()
+{
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
+// Block until the grids this one depends on have completed and their
+// memory operations are visible (no-op when it was launched normally).
+__device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
 // ------------------------------------------------------------- mbarrier ----
 
 __device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count)

@@ -97,6 +97,7 @@ __global__ void __launch_bounds__(256, 8) quant_rows_kernel(const uint16_t *__re
                                                             int64_t tiles_g, const int32_t *__restrict__ row_index,
                                                             int64_t n_src, int *status)
 {
+    griddep_launch_dependents();  // a dependent GEMM may set itself up under this grid's tail
     __shared__ float s_scale[QR_GROUPS][QR_ROWS];
     const int hw = threadIdx.x >> 4;
     const int l = threadIdx.x & 15;
@@ -169,6 +170,7 @@ __global__ void __launch_bounds__(256, 8) quant_rows_scatter_kernel(const uint16
                                                                     int64_t tiles_g, const int32_t *__restrict__ dest,
                                                                     int k, int64_t n_out, int *status)
 {
+    griddep_launch_dependents();  // a dependent GEMM may set itself up under this grid's tail
     __shared__ float s_scale[QR_GROUPS][QR_ROWS];
     __shared__ int32_t s_dst[QR_ROWS][SCATTER_MAX_K];
     const int hw = threadIdx.x >> 4;
@@ -241,6 +243,7 @@ __global__ void __launch_bounds__(256, 8) quant_cols_t_kernel(const uint16_t *__
                                                            int64_t cols, int64_t ldx, uint8_t *__restrict__ qT,
                                                            int64_t ldq, float *__restrict__ scales, int64_t ld_s)
 {
+    griddep_launch_dependents();  // a dependent GEMM may set itself up under this grid's tail
     __shared__ __align__(16) uint16_t tile[GROUP][QT_COLS];
     __shared__ uint32_t s_amax[4][QT_COLS];
     const int tid = threadIdx.x;
@@ -307,6 +310,7 @@ __global__ void __launch_bounds__(256, 5) quant_dual_kernel(const uint16_t *__re
                                                             uint8_t *__restrict__ qT, int64_t ldqT,
                                                             float *__restrict__ scalesT, int64_t ld_sT)
 {
+    griddep_launch_dependents();  // a dependent GEMM may set itself up under this grid's tail
     __shared__ __align__(16) uint16_t tile[GROUP][GROUP];
     __shared__ uint32_t s_amax[2][GROUP];
     __shared__ float s_row[GROUP];
@@ -381,6 +385,7 @@ __global__ void __launch_bounds__(256) quant_blocks_kernel(const uint16_t *__res
                                                            uint8_t *__restrict__ q, int64_t ldq,
                                                            float *__restrict__ scales)
 {
+    griddep_launch_dependents();  // a dependent GEMM may set itself up under this grid's tail
     __shared__ uint32_t s_warp[8];
     const int tid = threadIdx.x;
     const int64_t bj = blockIdx.x, bi = blockIdx.y;
