@@ -75,16 +75,33 @@ __device__ __forceinline__ uint4 ld_stream_v4(const void *p)
 }
 
 // ------------------------------------------------------ 1x128, per row ----
-// CTA tile: 4 rows x 16 groups (2048 columns); 256 threads = 16 half-warps.
+// CTA tile: 4 rows x gt groups (gt <= 16; 16 gt threads = gt half-warps).
 // Half-warp h owns group h of the tile and quantises it in each of the 4
 // rows, loading all four 256-byte segments before reducing any. The grid
 // walks the tiles in memory order (group blocks fastest). Small CTAs with
-// few registers keep eight per SM resident, which keeps enough loads in
-// flight to stream at HBM rate; a sweep of tile shapes on GB300 put this
-// one ahead of taller tiles with more loads per thread.
+// few registers keep eight or more per SM resident, which keeps enough
+// loads in flight to stream at HBM rate; a sweep of tile shapes on GB300
+// put 4 rows ahead of taller tiles with more loads per thread. The host
+// picks gt so that it divides the row's group count where it can (14 for
+// 56 groups): a partly empty last tile in every row would leave its
+// half-warps idle.
 constexpr int QR_ROWS = 4;
-constexpr int QR_GROUPS = 16;
-constexpr int QR_ITEMS = QR_ROWS * QR_GROUPS / 16;
+constexpr int QR_GROUPS = 16;  // largest group tile
+constexpr int QR_ITEMS = QR_ROWS;
+
+// Groups per tile for a row of ngroups groups: the largest even width from 8
+// to 16 that divides ngroups, else 16; short rows take one tile of ngroups
+// rounded up to even. The width is even so that every warp of the CTA is
+// whole (the reductions shuffle across full warps).
+inline int row_group_tile(int64_t ngroups)
+{
+    if (ngroups <= QR_GROUPS)
+        return (int)((ngroups + 1) & ~int64_t(1));
+    for (int g = QR_GROUPS; g >= 8; g -= 2)
+        if (ngroups % g == 0)
+            return g;
+    return QR_GROUPS;
+}
 
 // GATHER: output row r quantises source row row_index[r] (rows listed in
 // MoE expert order); an index outside [0, n_src) is reported as
@@ -94,7 +111,7 @@ template <bool GATHER, bool P2>
 __global__ void __launch_bounds__(256, 8) quant_rows_kernel(const uint16_t *__restrict__ x, int64_t rows,
                                                             int64_t ngroups, int64_t ldx, uint8_t *__restrict__ q,
                                                             int64_t ldq, float *__restrict__ scales, int64_t ld_s,
-                                                            int64_t tiles_g, const int32_t *__restrict__ row_index,
+                                                            int64_t tiles_g, int gt, const int32_t *__restrict__ row_index,
                                                             int64_t n_src, int *status)
 {
     griddep_launch_dependents();  // a dependent GEMM may set itself up under this grid's tail
@@ -103,7 +120,7 @@ __global__ void __launch_bounds__(256, 8) quant_rows_kernel(const uint16_t *__re
     const int l = threadIdx.x & 15;
     const int64_t gb = blockIdx.x % tiles_g, rb = blockIdx.x / tiles_g;
     const int64_t r0 = rb * QR_ROWS;
-    const int64_t g = gb * QR_GROUPS + hw;
+    const int64_t g = gb * gt + hw;
     const bool g_ok = g < ngroups;
     const uint16_t *src = x + r0 * ldx + g * GROUP + l * 8;
     uint8_t *dst = q + r0 * ldq + g * GROUP + l * 8;
@@ -145,9 +162,9 @@ __global__ void __launch_bounds__(256, 8) quant_rows_kernel(const uint16_t *__re
         }
     }
     __syncthreads();
-    if (threadIdx.x < QR_ROWS * QR_GROUPS) {
+    if (threadIdx.x < QR_ROWS * gt) {
         const int gg = threadIdx.x / QR_ROWS, rr = threadIdx.x % QR_ROWS;
-        const int64_t row = r0 + rr, gs = gb * QR_GROUPS + gg;
+        const int64_t row = r0 + rr, gs = gb * gt + gg;
         if (row < rows && gs < ngroups)
             scales[gs * ld_s + row] = s_scale[gg][rr];
     }
@@ -167,7 +184,7 @@ __global__ void __launch_bounds__(256, 8) quant_rows_scatter_kernel(const uint16
                                                                     int64_t ngroups, int64_t ldx,
                                                                     uint8_t *__restrict__ q, int64_t ldq,
                                                                     float *__restrict__ scales, int64_t ld_s,
-                                                                    int64_t tiles_g, const int32_t *__restrict__ dest,
+                                                                    int64_t tiles_g, int gt, const int32_t *__restrict__ dest,
                                                                     int k, int64_t n_out, int *status)
 {
     griddep_launch_dependents();  // a dependent GEMM may set itself up under this grid's tail
@@ -177,7 +194,7 @@ __global__ void __launch_bounds__(256, 8) quant_rows_scatter_kernel(const uint16
     const int l = threadIdx.x & 15;
     const int64_t gb = blockIdx.x % tiles_g, rb = blockIdx.x / tiles_g;
     const int64_t r0 = rb * QR_ROWS;
-    const int64_t g = gb * QR_GROUPS + hw;
+    const int64_t g = gb * gt + hw;
     const bool g_ok = g < ngroups;
     if (threadIdx.x < QR_ROWS * k) {
         const int rr = threadIdx.x / k, j = threadIdx.x % k;
@@ -221,10 +238,10 @@ __global__ void __launch_bounds__(256, 8) quant_rows_scatter_kernel(const uint16
         }
     }
     __syncthreads();
-    for (int idx = threadIdx.x; idx < QR_GROUPS * QR_ROWS * k; idx += blockDim.x) {
+    for (int idx = threadIdx.x; idx < gt * QR_ROWS * k; idx += blockDim.x) {
         const int gg = idx / (QR_ROWS * k), rem = idx % (QR_ROWS * k);
         const int rr = rem / k, j = rem % k;
-        const int64_t gs = gb * QR_GROUPS + gg;
+        const int64_t gs = gb * gt + gg;
         const int32_t d = s_dst[rr][j];
         if (r0 + rr < rows && gs < ngroups && d >= 0)
             scales[gs * ld_s + d] = s_scale[gg][rr];
@@ -450,13 +467,14 @@ int quant_1x128(const void *x, int64_t rows, int64_t cols, int64_t ldx, uint8_t 
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     if (transpose == 0) {
         const int64_t ngroups = cols / GROUP;
-        const int64_t tiles_g = (ngroups + QR_GROUPS - 1) / QR_GROUPS;
+        const int gt = row_group_tile(ngroups);
+        const int64_t tiles_g = (ngroups + gt - 1) / gt;
         const int64_t tiles = tiles_g * ((rows + QR_ROWS - 1) / QR_ROWS);
         if (tiles > 0x7FFFFFFF)
             return FP8FG_EINVAL;
-        quant_rows_kernel<false, P2><<<(unsigned)tiles, 256, 0, s>>>(static_cast<const uint16_t *>(x), rows, ngroups,
-                                                                  ldx, q, ldq, scales, ld_s, tiles_g, nullptr, 0,
-                                                                  nullptr);
+        quant_rows_kernel<false, P2><<<(unsigned)tiles, 16 * gt, 0, s>>>(static_cast<const uint16_t *>(x), rows,
+                                                                      ngroups, ldx, q, ldq, scales, ld_s, tiles_g,
+                                                                      gt, nullptr, 0, nullptr);
     } else {
         const int64_t gx = (cols + QT_COLS - 1) / QT_COLS, gy = rows / GROUP;
         if (gx > 0x7FFFFFFF || gy > 65535)
@@ -486,12 +504,13 @@ int quant_1x128_gather(const void *x, int64_t n_src, int64_t cols, int64_t ldx,
     if (!status)
         return FP8FG_ECUDA;
     const int64_t ngroups = cols / GROUP;
-    const int64_t tiles_g = (ngroups + QR_GROUPS - 1) / QR_GROUPS;
+    const int gt = row_group_tile(ngroups);
+    const int64_t tiles_g = (ngroups + gt - 1) / gt;
     const int64_t tiles = tiles_g * ((rows + QR_ROWS - 1) / QR_ROWS);
     if (tiles > 0x7FFFFFFF)
         return FP8FG_EINVAL;
-    quant_rows_kernel<true, P2><<<(unsigned)tiles, 256, 0, static_cast<cudaStream_t>(stream)>>>(
-        static_cast<const uint16_t *>(x), rows, ngroups, ldx, q, ldq, scales, ld_s, tiles_g, row_index, n_src,
+    quant_rows_kernel<true, P2><<<(unsigned)tiles, 16 * gt, 0, static_cast<cudaStream_t>(stream)>>>(
+        static_cast<const uint16_t *>(x), rows, ngroups, ldx, q, ldq, scales, ld_s, tiles_g, gt, row_index, n_src,
         status);
     return launch_status();
 }
@@ -515,13 +534,14 @@ int quant_1x128_scatter(const void *x, int64_t n_src, int64_t cols, int64_t ldx,
     if (!status)
         return FP8FG_ECUDA;
     const int64_t ngroups = cols / GROUP;
-    const int64_t tiles_g = (ngroups + QR_GROUPS - 1) / QR_GROUPS;
+    const int gt = row_group_tile(ngroups);
+    const int64_t tiles_g = (ngroups + gt - 1) / gt;
     const int64_t tiles = tiles_g * ((n_src + QR_ROWS - 1) / QR_ROWS);
     if (tiles > 0x7FFFFFFF)
         return FP8FG_EINVAL;
-    quant_rows_scatter_kernel<P2><<<(unsigned)tiles, 256, 0, static_cast<cudaStream_t>(stream)>>>(
-        static_cast<const uint16_t *>(x), n_src, ngroups, ldx, q, ldq, scales, ld_s, tiles_g, dest_index, k, n_out,
-        status);
+    quant_rows_scatter_kernel<P2><<<(unsigned)tiles, 16 * gt, 0, static_cast<cudaStream_t>(stream)>>>(
+        static_cast<const uint16_t *>(x), n_src, ngroups, ldx, q, ldq, scales, ld_s, tiles_g, gt, dest_index, k,
+        n_out, status);
     return launch_status();
 }
 
