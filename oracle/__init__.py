@@ -51,6 +51,7 @@ def lib():
         L.orc_quant_128x128_rule.argtypes = [P, I64, I64, P, P, ctypes.c_int]
         L.orc_gemm_blockscaled.argtypes = [P, P, P, P, I64, I64, I64, P, I64, P, P, P]
         L.orc_f32_to_bf16.argtypes = [P, I64, P]
+        L.orc_moe_combine.argtypes = [P, I64, P, P, I64, ctypes.c_int, I64, P, ctypes.c_int]
         L.orc_num_threads.restype = ctypes.c_int
         L.orc_set_num_threads.argtypes = [ctypes.c_int]
         _lib = L
@@ -260,4 +261,22 @@ def to_bf16_bits(c):
     c = _c(c, np.float32)
     out = np.empty(c.shape, np.uint16)
     lib().orc_f32_to_bf16(_ptr(c), c.size, _ptr(out))
+    return out
+
+
+def moe_combine(y_bits, dest, w, out_f32=False):
+    """MoE combine: out[t] = sum_{j<k} w[t, j] * y[dest[t, j]] (FP32 products
+    and sums in slot order, no FMA; slots with dest < 0 skipped), rounded to
+    bf16 bits (or FP32 with out_f32). y_bits uint16 bf16 bit patterns
+    [rows, N]; dest int32 [T, k]; w float32 [T, k]."""
+    y = _c(y_bits, np.uint16)
+    d = _c(dest, np.int32)
+    ww = _c(w, np.float32)
+    T, k = d.shape
+    assert ww.shape == (T, k)
+    N = y.shape[1]
+    assert d.size == 0 or d.max() < y.shape[0]
+    out = np.empty((T, N), np.float32 if out_f32 else np.uint16)
+    if T and N:
+        lib().orc_moe_combine(_ptr(y), N, _ptr(d), _ptr(ww), T, k, N, _ptr(out), 1 if out_f32 else 0)
     return out

@@ -366,6 +366,47 @@ void orc_f32_to_bf16(const float *v, int64_t n, uint16_t *out)
     }
 }
 
+/*
+ * MoE combine: the output of token t is the gate-weighted sum of the rows
+ * its k routed experts produced for it,
+ *     out[t][n] = sum_{j < k} w[t][j] * y[dest[t][j]][n],
+ * the MoE layer's definition, with the expert rows dispatched in FP8 and
+ * returned in bf16 ([innerforce], the mixed-precision framework paragraph:
+ * activations are cached and dispatched in FP8; [yunhecapital 2.2.2] and
+ * [tonho] "como funciona": 8 of 256 routed experts per token). The pages fix
+ * no precision for the combine. Reading: y is bf16 (the experts' output
+ * format), each product w*y and each partial sum an IEEE FP32 operation in
+ * slot order j = 0, 1, ..., k-1 (no fused multiply-add), slots with
+ * dest < 0 skipped, then the FP32 sum rounded to bf16 (nearest even) or
+ * kept in FP32 when out_f32 is set.
+ *   y    bf16 bits [rows][ldy]; dest int32 [T][k]; w FP32 [T][k]
+ *   out  bf16 bits [T][N] (out_f32 = 0) or FP32 [T][N] (out_f32 = 1)
+ */
+void orc_moe_combine(const uint16_t *y, int64_t ldy, const int32_t *dest, const float *w, int64_t T, int k,
+                     int64_t N, void *out, int out_f32)
+{
+#pragma omp parallel for schedule(static)
+    for (int64_t t = 0; t < T; ++t) {
+        for (int64_t n = 0; n < N; ++n) {
+            float acc = 0.0f;
+            for (int j = 0; j < k; ++j) {
+                const int32_t d = dest[t * k + j];
+                if (d < 0)
+                    continue;
+                uint32_t u = (uint32_t)y[(int64_t)d * ldy + n] << 16;
+                float v;
+                memcpy(&v, &u, sizeof v);
+                const float prod = w[t * k + j] * v;
+                acc = acc + prod;
+            }
+            if (out_f32)
+                ((float *)out)[t * N + n] = acc;
+            else
+                orc_f32_to_bf16(&acc, 1, (uint16_t *)out + t * N + n);
+        }
+    }
+}
+
 int orc_version(void) { return 1; }
 
 /* Threads the following OpenMP regions of this library use (n >= 1); for
