@@ -32,7 +32,7 @@ dirty lines are written back inside the next step), outside the events.
 
 Usage:
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
-                    [--workload dense|trio|moe|outliers|tiny|dense_e4m3|dense_mx|trio_mx|moe_mx]
+                    [--workload dense|trio|moe|moe_layer|outliers|tiny|dense_e4m3|dense_mx|trio_mx|moe_mx]
 Under torchrun (N > 1) every rank runs its own replica of the workload
 (weak scaling, no data-path collective); times are the max over ranks.
 ``--impl reference`` times the CPU oracle on a bounded sample of the same
@@ -69,6 +69,9 @@ WORKLOADS = {
                   "next layer's input): quant X 1x128 + GEMM, M=4096 K=7168 N=7168",
     "dense_mx": "dense projection fprop, microscaling variant (power-of-two scales, tensor-core block "
                 "scaling): quant 1x128 + GEMM, M=4096 K=7168 N=7168, bf16 out",
+    "moe_layer": "MoE layer forward on one GPU: 4096 tokens, 256 experts 2048x7168, top-8 with Zipf(1.1) bias; "
+                 "FP8 dispatch (each token quantised once into its 8 expert-order rows) + grouped GEMM + "
+                 "gate-weighted combine of the 8 bf16 expert rows",
     "moe_mx": "MoE experts, microscaling variant (power-of-two scales, tensor-core block scaling): 4096 tokens, "
               "256 experts 2048x7168, top-8 with Zipf(1.1) bias; quant X into expert order + grouped GEMM",
     "trio_mx": "linear 7168->18432 at M=8192, microscaling variant (power-of-two scales, tensor-core block "
@@ -318,6 +321,41 @@ def build(workload, dev, seed, fg, synth):
             Part("wgrad", gk + "<WGRAD>", lambda: gemm(fg.WGRAD, dyqT, sdyT, xqT, sxT, c=dw), "tensor", f),
         ]
         W.update(inputs=[x, dy], outputs=[y, dx, dw], flops=3 * f, dims={"M": Mx, "K": Kx, "N": Nw})
+    elif workload == "moe_layer":
+        from fp8_fine_grained_gb300 import ep
+        mo = synth.moe(seed=seed, device=dev, make_weights=False)
+        E, Nw, Kx = 256, 2048, mo.x.shape[1]
+        wq = torch.empty((E, Nw, Kx), dtype=torch.uint8, device=dev)
+        sw = torch.empty((E, Nw // 128, Kx // 128), dtype=torch.float32, device=dev)
+        g = torch.Generator(device=dev)
+        g.manual_seed(seed + 1)
+        for e in range(E):
+            we = (torch.randn(Nw, Kx, generator=g, device=dev) * 0.02).to(torch.bfloat16)
+            fg.fp8_quant_128x128(we, q=wq[e], scales=sw[e])
+        T, topk = mo.topk_ids.shape
+        plan = ep.plan_dispatch(mo.topk_ids, E, 1)      # rows by (expert, token): the routing's row order
+        R = plan.n_send
+        off = torch.zeros(E + 1, dtype=torch.int32, device=dev)
+        off[1:] = torch.cumsum(plan.send_counts[0], 0).to(torch.int32)
+        dest, gates = plan.dest, mo.gates
+        xg = torch.empty((R, Kx), dtype=torch.uint8, device=dev)
+        sxg = torch.empty((Kx // 128, R), dtype=torch.float32, device=dev)
+        y = torch.empty((R, Nw), dtype=torch.bfloat16, device=dev)
+        out = torch.empty((T, Nw), dtype=torch.bfloat16, device=dev)
+        nonempty = int((plan.send_counts[0] > 0).sum().item())
+        moved = nonempty * Nw * Kx + R * Kx + R * Nw * 2 + sw.numel() * 4 + R * (Kx // 128) * 4
+        f = 2.0 * R * Nw * Kx
+        parts = [
+            Part("quant_x_scatter", "quant_rows_scatter_kernel",
+                 lambda: fg.fp8_quant_1x128_scatter(mo.x, dest, R, q=xg, scales=sxg), "hbm",
+                 2 * T * Kx + (Q1X128_B - 2) * R * Kx + 4 * R),
+            Part("grouped", "gemm_kernel<GROUPED_C>",
+                 lambda: fg.fp8_grouped_gemm(xg, sxg, None, off, wq, sw, R, y=y), "tensor", f, extra_bytes=moved),
+            Part("combine", "moe_combine_kernel",
+                 lambda: fg.fp8_moe_combine(y, dest, gates, out=out), "hbm", 2 * R * Nw + 2 * T * Nw + 8 * T * topk),
+        ]
+        W.update(inputs=[mo.x, dest, gates], outputs=[out], flops=f,
+                 dims={"tokens": T, "experts": E, "N": Nw, "K": Kx, "rows": R, "nonempty_experts": nonempty})
     elif workload == "moe":
         mo = synth.moe(seed=seed, device=dev, make_weights=False)
         E, Nw, Kx = 256, 2048, mo.x.shape[1]
@@ -365,7 +403,7 @@ def build(workload, dev, seed, fg, synth):
 
 def kernel_source_sha():
     h = hashlib.sha256()
-    for f in ("gemm.cu", "gemm_mx.cu", "quant.cu", "ptx.cuh", "group_rule.cuh"):
+    for f in ("gemm.cu", "gemm_mx.cu", "quant.cu", "moe.cu", "ptx.cuh", "group_rule.cuh"):
         with open(os.path.join(ROOT, "fp8_fine_grained_gb300", "csrc", f), "rb") as fh:
             h.update(fh.read())
     return h.hexdigest()[:16]
@@ -524,7 +562,7 @@ def e2e_run(W, args, dev, rank, fg, synth, pg):
 
 # the five workloads of the measurement plan; the headline is one of them,
 # the others are reported under "configs" on the same line
-CONFIG_SET = ("tiny", "dense", "trio", "moe", "outliers")
+CONFIG_SET = ("tiny", "dense", "trio", "moe", "moe_layer", "outliers")
 
 
 def run_ours(args):
@@ -702,7 +740,8 @@ def config_of(workload, world):
 def oracle_dims(workload):
     """(M, K, N) of the workload's first GEMM, the one the CPU sample runs."""
     return {"dense": (4096, 7168, 7168), "dense_e4m3": (4096, 7168, 7168), "outliers": (16384, 7168, 7168),
-            "trio": (8192, 7168, 18432), "moe": (32768, 7168, 2048), "tiny": (128, 256, 128),
+            "trio": (8192, 7168, 18432), "moe": (32768, 7168, 2048), "moe_layer": (32768, 7168, 2048),
+            "tiny": (128, 256, 128),
             "dense_mx": (4096, 7168, 7168), "trio_mx": (8192, 7168, 18432), "moe_mx": (32768, 7168, 2048)}[workload]
 
 

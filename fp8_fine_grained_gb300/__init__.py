@@ -56,6 +56,7 @@ def lib():
         L.fp8_gemm_blockscaled.argtypes = [I32, P, P, I64, I64, P, P, I64, I64, I64, I64, I64, P, I32, I64, P]
         L.fp8_gemm_blockscaled_e4m3.argtypes = [I32, P, P, I64, I64, P, P, I64, I64, I64, I64, I64, P, I64, P, I64, P]
         L.fp8_grouped_gemm.argtypes = [P, P, I64, I64, P, P, ctypes.c_int32, I64, P, P, I64, I64, P, I32, I64, P]
+        L.fp8_moe_combine.argtypes = [P, I64, I64, P, P, I64, I32, I64, P, I32, I64, P]
         L.fp8fg_status_str.argtypes = [I32]
         L.fp8fg_status_str.restype = ctypes.c_char_p
         L.fp8fg_device_status.argtypes = [P]
@@ -498,6 +499,33 @@ def fp8_grouped_gemm_mx(xq, sx, expert_offsets, wq, sw, n_rows, out_dtype=None, 
                                    _ptr(sw), N, K, _ptr(y), _out_code(y.dtype), y.stride(0), _stream(stream))
     _check(rc, "fp8_grouped_gemm_mx")
     return y
+
+
+def fp8_moe_combine(y, dest, w, out_dtype=None, out=None, stream=None):
+    """MoE combine: out[t] = sum_{j<k} w[t, j] * y[dest[t, j]] with FP32
+    products and sums in slot order (no FMA); a negative dest skips the
+    slot. y bf16 [rows, N]; dest int32 [T, k]; w float32 [T, k]; returns
+    out [T, N] (bf16 by default, or float32)."""
+    torch = _torch()
+    _layout(y, "y")
+    _dtype(y, torch.bfloat16, "y")
+    _dtype(dest, torch.int32, "dest")
+    _dtype(w, torch.float32, "w")
+    if dest.dim() != 2 or not dest.is_contiguous() or not w.is_contiguous() or tuple(w.shape) != tuple(dest.shape):
+        raise ValueError("dest and w must be contiguous [T, k] tensors of the same shape")
+    T, k = dest.shape
+    N = y.shape[1]
+    if out_dtype is None:
+        out_dtype = torch.bfloat16 if out is None else out.dtype
+    if out is None:
+        out = torch.empty((T, N), dtype=out_dtype, device=y.device)
+    _layout(out, "out")
+    _at_least(out, T, N, "out")
+    _on_gpu((y, "y"), (dest, "dest"), (w, "w"), (out, "out"))
+    rc = lib().fp8_moe_combine(_ptr(y), y.stride(0), y.shape[0], _ptr(dest), _ptr(w), T, k, N, _ptr(out),
+                               _out_code(out.dtype), out.stride(0), _stream(stream))
+    _check(rc, "fp8_moe_combine")
+    return out
 
 
 def device_status(stream=None):

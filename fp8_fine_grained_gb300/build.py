@@ -15,7 +15,7 @@ CSRC = os.path.join(HERE, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(HERE, "libfp8fg.so")
-SOURCES = ["capi.cu", "quant.cu", "gemm.cu", "gemm_mx.cu"]
+SOURCES = ["capi.cu", "quant.cu", "gemm.cu", "gemm_mx.cu", "moe.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-Xcompiler", "-Wall", "-Xcompiler", "-fvisibility=hidden",
               "--expt-relaxed-constexpr", "-I", INCLUDE, "-I", CSRC]

@@ -1,0 +1,180 @@
+"""Expert-parallel FP8 dispatch and combine for an MoE layer.
+
+The pages' MoE layer routes every token to 8 of 256 experts
+(yunhecapital.com 2.2.2; tonho.wtf "como funciona"), and to cut memory and
+communication the activations are cached and dispatched to the experts in
+FP8 (innerforce.co.kr, the mixed-precision framework paragraph;
+yunhecapital.com 2.2.3); the experts' outputs come back in bf16 and are
+combined with the gate weights. With experts spread over ranks (expert
+parallelism) the dispatch and the return are all-to-all exchanges.
+
+Ranks and experts: R ranks, E experts; rank r owns experts
+[r * E/R, (r + 1) * E/R). Every rank holds its own T tokens with top-k
+expert ids and gate weights.
+
+One layer, per rank:
+
+1. plan_dispatch: every (token t, slot j) becomes one row of the send
+   buffer; rows are ordered by expert (so by destination rank too), then by
+   token and slot: a stable counting sort of the slots by expert id.
+   dest[t, j] is the row; send_counts[r, e] the rows for rank r's local
+   expert e.
+2. fp8_quant_1x128_scatter quantises every token once and writes its codes
+   and scales to its k send rows (library kernel).
+3. exchange_counts, then exchange_rows for the code rows and the scale rows
+   (torch.distributed.all_to_all_single: NCCL between GPUs, gloo in the CPU
+   tests). The scales travel token-major, [rows, K/128], one contiguous
+   run per destination.
+4. receive_layout: the received rows arrive grouped by source rank, each
+   source's rows grouped by expert; row_index lists them expert by expert
+   (sources ascending inside an expert) and expert_offsets bounds each
+   expert, the inputs of fp8_grouped_gemm's row-index mode.
+5. The expert GEMMs (fp8_grouped_gemm) write the outputs in expert order;
+   to_receive_order puts them back where the rows were received, and
+   exchange_rows returns them (the same splits, reversed), landing in the
+   send order.
+6. fp8_moe_combine: out[t] = sum_j w[t, j] * y[dest[t, j]] (library kernel).
+
+On one rank (world 1, moe_forward with pg=None) steps 3 and 5's reorder
+are identities: the send buffer is the expert GEMM's input, in expert
+order, and the combine reads the GEMM's output directly.
+
+What runs where: steps 1, 4 and 5's reorder are index bookkeeping and row
+moves in torch (no FP8 arithmetic), the exchanges are collectives, every
+quantisation, GEMM and combine is a library kernel. The multi-rank path is
+tested with two gloo ranks on the CPU (tests/test_ep_gloo.py, with the
+oracle standing in for the kernels); it has not run on more than one GPU.
+"""
+from collections import namedtuple
+
+Plan = namedtuple("Plan", "dest send_counts n_send")
+Layout = namedtuple("Layout", "row_index expert_offsets n_recv")
+
+
+def _torch():
+    import torch
+    return torch
+
+
+def plan_dispatch(topk_ids, n_experts, world):
+    """Send-buffer rows of every (token, slot).
+
+    topk_ids: int tensor [T, k] of global expert ids (a negative id means the
+    slot is unused). Returns Plan(dest int32 [T, k] (send row, -1 for unused
+    slots), send_counts int64 [world, E/world] (rows per destination rank and
+    local expert), n_send)."""
+    torch = _torch()
+    if n_experts % world != 0:
+        raise ValueError("the experts must split evenly over the ranks")
+    if topk_ids.dim() != 2:
+        raise ValueError("topk_ids must be [T, k]")
+    ids = topk_ids.reshape(-1).to(torch.int64)
+    valid = ids >= 0
+    if bool((ids >= n_experts).any()):
+        raise ValueError("expert id out of range")
+    key = torch.where(valid, ids, torch.full_like(ids, n_experts))   # unused slots sort last
+    order = torch.sort(key, stable=True).indices
+    row = torch.empty_like(order)
+    row[order] = torch.arange(order.numel(), device=ids.device)
+    n_send = int(valid.sum().item())
+    dest = torch.where(valid, row, torch.full_like(row, -1)).to(torch.int32).reshape(topk_ids.shape)
+    counts = torch.bincount(ids[valid], minlength=n_experts).reshape(world, n_experts // world)
+    return Plan(dest.contiguous(), counts, n_send)
+
+
+def exchange_counts(send_counts, pg=None):
+    """recv_counts [world, E/world]: row s = the rows source rank s sends to
+    this rank, per local expert."""
+    if pg is None:
+        return send_counts.clone()
+    torch = _torch()
+    recv = torch.empty_like(send_counts)
+    pg.all_to_all_single(recv, send_counts.contiguous())
+    return recv
+
+
+def exchange_rows(send, send_rows, recv_rows, pg=None):
+    """All-to-all of a row-major 2-D tensor: rows [sum(send_rows)] in
+    destination order -> rows [sum(recv_rows)] in source order (split sizes
+    per rank). The rows travel as bytes, whatever their element type."""
+    if pg is None:
+        return send
+    torch = _torch()
+    raw = send.contiguous().view(torch.uint8)
+    recv = torch.empty((int(sum(recv_rows)), raw.shape[1]), dtype=torch.uint8, device=send.device)
+    pg.all_to_all_single(recv, raw, output_split_sizes=[int(v) for v in recv_rows],
+                         input_split_sizes=[int(v) for v in send_rows])
+    return recv.view(send.dtype)
+
+
+def receive_layout(recv_counts, device=None):
+    """Expert-by-expert view of the received rows (sources ascending inside
+    an expert): Layout(row_index int32 [n_recv], expert_offsets int32
+    [E/world + 1], n_recv). Computed on the host from the count table (the
+    exchange needs the counts there too) and placed on `device`."""
+    import numpy as np
+    torch = _torch()
+    c = recv_counts.detach().to("cpu").to(torch.int64).numpy()        # [R, Er]
+    R, Er = c.shape
+    per_src = c.sum(1)
+    src_start = np.cumsum(per_src) - per_src                           # first row of each source's chunk
+    within = np.cumsum(c, 1) - c                                       # expert e's offset inside source s's chunk
+    starts = (src_start[:, None] + within).T.reshape(-1)               # runs in (expert, source) order
+    lens = c.T.reshape(-1)
+    n_recv = int(lens.sum())
+    run_first = np.cumsum(lens) - lens                                 # where each run begins in row_index
+    row_index = np.arange(n_recv, dtype=np.int64) - np.repeat(run_first, lens) + np.repeat(starts, lens)
+    offsets = np.zeros(Er + 1, np.int64)
+    offsets[1:] = np.cumsum(c.sum(0))
+    dev = recv_counts.device if device is None else device
+    return Layout(torch.from_numpy(row_index.astype(np.int32)).to(dev),
+                  torch.from_numpy(offsets.astype(np.int32)).to(dev), n_recv)
+
+
+def to_receive_order(y, row_index, n_recv):
+    """Rows of the expert GEMM's output (expert order) back to the order they
+    were received in: out[row_index[r]] = y[r]."""
+    torch = _torch()
+    out = torch.empty((n_recv,) + tuple(y.shape[1:]), dtype=y.dtype, device=y.device)
+    out.index_copy_(0, row_index.to(torch.int64), y)
+    return out
+
+
+def rank_rows(counts):
+    """Rows per rank of a [world, E/world] count table."""
+    return [int(v) for v in counts.sum(1).tolist()]
+
+
+def moe_forward(x, topk_ids, topk_w, wq, sw, n_experts, pg=None, world=1, out_dtype=None):
+    """One MoE layer forward with FP8 dispatch on the GPU: x bf16 [T, K];
+    topk_ids int [T, k]; topk_w float32 [T, k]; wq uint8 [E/world, N, K] and
+    sw float32 [E/world, N/128, K/128], this rank's experts (128x128
+    quantised). Returns out [T, N] (bf16 by default)."""
+    import fp8_fine_grained_gb300 as fg
+    torch = _torch()
+    plan = plan_dispatch(topk_ids, n_experts, world)
+    K = x.shape[1]
+    q_send, s_send = fg.fp8_quant_1x128_scatter(x, plan.dest, max(plan.n_send, 1))
+    if pg is None:
+        # one rank: the send buffer is already in expert order
+        y = fg.fp8_grouped_gemm(q_send, s_send, None, _offsets(plan.send_counts[0], x.device), wq, sw,
+                                plan.n_send)
+        return fg.fp8_moe_combine(y, plan.dest, topk_w, out_dtype=out_dtype)
+    recv_counts = exchange_counts(plan.send_counts, pg)
+    srows, rrows = rank_rows(plan.send_counts), rank_rows(recv_counts)
+    q_recv = exchange_rows(q_send[:plan.n_send], srows, rrows, pg)
+    s_recv = exchange_rows(s_send[:, :plan.n_send].t().contiguous(), srows, rrows, pg)
+    lay = receive_layout(recv_counts, x.device)
+    ld = (max(lay.n_recv, 1) + 3) // 4 * 4
+    s_cols = torch.zeros((K // 128, ld), dtype=torch.float32, device=x.device)
+    s_cols[:, :lay.n_recv] = s_recv.t()
+    y = fg.fp8_grouped_gemm(q_recv, s_cols, lay.row_index, lay.expert_offsets, wq, sw, lay.n_recv)
+    y_back = exchange_rows(to_receive_order(y, lay.row_index, lay.n_recv), rrows, srows, pg)
+    return fg.fp8_moe_combine(y_back, plan.dest, topk_w, out_dtype=out_dtype)
+
+
+def _offsets(counts, device):
+    torch = _torch()
+    off = torch.zeros(counts.numel() + 1, dtype=torch.int32, device=device)
+    off[1:] = torch.cumsum(counts.to(torch.int64), 0).to(torch.int32)
+    return off

@@ -102,6 +102,8 @@ class MoEInputs:
     row_index: torch.Tensor    # int32 [T*topk]: token of each expert row, grouped by expert
     expert_offsets: torch.Tensor  # int32 [E+1]
     counts: torch.Tensor       # int64 [E]
+    topk_ids: torch.Tensor = None  # int32 [T, topk]: each token's experts, best first
+    gates: torch.Tensor = None     # float32 [T, topk]: softmax of the chosen experts' logits (no bias)
 
 
 def route_topk(logits, bias, topk):
@@ -136,7 +138,13 @@ def moe(seed=0, device="cpu", T=4096, K=HIDDEN, N=2048, E=256, topk=8, zipf_s=1.
     bias = -zipf_s * torch.log(ranks)
     w = normal((E, N, K), 0.02, g, device) if make_weights else None
     row_index, off, counts = route_topk(logits, bias, topk)
-    return MoEInputs(to_bf16(x), to_bf16(w) if w is not None else None, row_index, off, counts)
+    # the combine's gate weights: the chosen experts ranked as route_topk
+    # ranks them, weighted by the softmax of their own logits (the per-expert
+    # bias only enters the choice); no further random draws
+    ids = torch.sort(-(logits + bias).float(), dim=1, stable=True).indices[:, :topk]
+    gates = torch.softmax(torch.gather(logits.float(), 1, ids), dim=1)
+    return MoEInputs(to_bf16(x), to_bf16(w) if w is not None else None, row_index, off, counts,
+                     ids.to(torch.int32).contiguous(), gates.contiguous())
 
 
 def bf16_bits(t):

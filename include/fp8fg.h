@@ -362,6 +362,35 @@ FP8FG_API int fp8_gemm_mx(int mode,
                          void *C, int out, int64_t ldc, void *stream);
 
 /* ---------------------------------------------------------------------
+ * fp8_moe_combine: the MoE layer's output from its experts' rows.
+ * Source: yunhecapital.com 2.2.2 and tonho.wtf "como funciona" (8 of 256
+ * routed experts per token: a token's output is the gate-weighted sum of
+ * its routed experts' outputs); innerforce.co.kr, the mixed-precision
+ * framework paragraph (activations are dispatched to the experts in FP8;
+ * the expert outputs come back in bf16). The pages fix no precision for
+ * the combine; the reading taken: FP32 products and sums in slot order.
+ *
+ *   out[t][n] = sum_{j < k} w[t][j] * y[dest[t][j]][n]
+ *   y       bf16 [y_rows][ldy] (for example fp8_grouped_gemm's output).
+ *   dest    int32 [T][k], device: row of y for token t's slot j; a negative
+ *           entry skips the slot (a token routed to fewer experts); an entry
+ *           >= y_rows is reported as FP8FG_EDEVICE through
+ *           fp8fg_device_status and skipped.
+ *   w       FP32 [T][k], device: gate weights.
+ *   out     [T][ldo], FP32 or bf16 per out_kind (FP8FG_OUT_F32 or
+ *           FP8FG_OUT_BF16; bf16: the FP32 sum
+ *           rounded to nearest even).
+ *   Each product w*y and each partial sum is an IEEE FP32 operation, in
+ *   slot order j = 0..k-1, with no fused multiply-add, so the result does
+ *   not depend on the launch.
+ *   1 <= k <= 16, N % 8 == 0, ldy >= N, ldo >= N.
+ *   Alignment: y and out 16-byte aligned, ldy % 8 == 0,
+ *   ldo*sizeof(out) % 16 == 0. T == 0 or N == 0 is a no-op.
+ * ------------------------------------------------------------------- */
+FP8FG_API int fp8_moe_combine(const void *y, int64_t ldy, int64_t y_rows, const int32_t *dest, const float *w,
+                    int64_t T, int k, int64_t N, void *out, int out_kind, int64_t ldo, void *stream);
+
+/* ---------------------------------------------------------------------
  * fp8_grouped_gemm_mx: the MoE expert GEMM of fp8_grouped_gemm (rows
  * already in expert order, i.e. row_index = NULL) for power-of-two scales,
  * on the tensor cores' block-scaled MMA as fp8_gemm_mx.

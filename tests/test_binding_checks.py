@@ -146,3 +146,15 @@ def test_grouped_tile_count_limit_in_the_abi():
     assert rc == 1  # FP8FG_EINVAL
     rc = L.fp8_grouped_gemm_mx(A16, A16, n_rows, A16, E, n_rows, A16, A16, N, K, A16, 1, N, None)
     assert rc == 1
+
+
+def test_combine_argument_checks():
+    y = z((100, 256), BF16)
+    dest = z((64, 8), I32)
+    w = z((64, 8), F32)
+    expect("CUDA tensor", fg.fp8_moe_combine, y, dest, w)
+    expect("y must be", fg.fp8_moe_combine, y.to(F32), dest, w)
+    expect("dest must be", fg.fp8_moe_combine, y, dest.to(torch.int64), w)
+    expect("w must be", fg.fp8_moe_combine, y, dest, w.to(BF16))
+    expect("same shape", fg.fp8_moe_combine, y, dest, w[:, :4].contiguous())
+    expect("out must cover", fg.fp8_moe_combine, y, dest, w, out=z((63, 256), BF16))

@@ -284,3 +284,26 @@ def test_quant_scatter_validation(L):
     assert call() in (EUNSUPPORTED, 4)
     args = (A16, 64, 256, 256, A16, 8, 512, A16, 256, A16, 500, NULL)
     assert L.fp8_quant_1x128_scatter_pow2(*args) == f(*args) == EINVAL
+
+
+def test_moe_combine_validation(L):
+    f = L.fp8_moe_combine
+
+    def call(**kw):
+        a = dict(y=A16, ldy=256, rows=100, d=A16, w=A16, T=64, k=8, N=256, out=A16, kind=1, ldo=256)
+        a.update(kw)
+        return f(a["y"], a["ldy"], a["rows"], a["d"], a["w"], a["T"], a["k"], a["N"], a["out"], a["kind"],
+                 a["ldo"], NULL)
+
+    assert call(k=0) == EINVAL
+    assert call(k=17) == EINVAL
+    assert call(N=100, ldy=104, ldo=104) == EINVAL   # N % 8 != 0
+    assert call(ldy=248) == EINVAL                   # ldy < N
+    assert call(ldo=248) == EINVAL                   # ldo < N
+    assert call(kind=2) == EINVAL
+    assert call(d=NULL) == EINVAL
+    assert call(y=A8) == EALIGN
+    assert call(ldy=260) == EALIGN                   # rows not 16-byte aligned
+    assert call(T=0) == 0
+    assert call(N=0, ldy=0, ldo=0) == 0
+    assert call() in (EUNSUPPORTED, 4)
