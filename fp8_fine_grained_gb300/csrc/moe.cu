@@ -10,10 +10,12 @@
 // fused multiply-add), then rounded to bf16 (nearest even) or kept in FP32.
 //
 // A memory stream (k bf16 rows read, one row written per token): each thread
-// owns 8 consecutive columns of one token, issues the k 16-byte loads of its
-// slots before it folds any, and writes 16 (bf16) or 32 (FP32) bytes. The
-// slot indices and gate weights of the token are read through the read-only
-// cache (every thread of the token reads the same k pairs).
+// owns 8 consecutive columns of one token and takes its slots in batches of
+// 8, issuing a batch's 16-byte loads before it folds any; the batch bounds
+// the registers so that four 256-thread CTAs fit on an SM (1024 threads with
+// 128 bytes each in flight). Each thread writes 16 (bf16) or 32 (FP32)
+// bytes. The slot indices and gate weights of the token are read through the
+// read-only cache (every thread of the token reads the same k pairs).
 #include <cuda_bf16.h>
 
 #include "host_common.h"
@@ -23,55 +25,59 @@ namespace fp8fg {
 namespace {
 
 constexpr int COMBINE_MAX_K = 16;
+constexpr int COMBINE_BATCH = 8;
 constexpr int COMBINE_THREADS = 256;
+constexpr int COMBINE_CTAS_PER_SM = 4;
 
 template <bool F32>
-__global__ void __launch_bounds__(COMBINE_THREADS) moe_combine_kernel(const uint16_t *__restrict__ y, int64_t ldy,
-                                                                      int64_t y_rows, const int32_t *__restrict__ dest,
-                                                                      const float *__restrict__ w, int64_t T, int k,
-                                                                      int64_t chunks, void *__restrict__ out,
-                                                                      int64_t ldo, int *status)
+__global__ void __launch_bounds__(COMBINE_THREADS, COMBINE_CTAS_PER_SM)
+    moe_combine_kernel(const uint16_t *__restrict__ y, int64_t ldy, int64_t y_rows, const int32_t *__restrict__ dest,
+                       const float *__restrict__ w, int64_t T, int k, int64_t chunks, void *__restrict__ out,
+                       int64_t ldo, int *status)
 {
     const int64_t total = T * chunks;
+    const int64_t ldy16 = ldy / 8;  // row pitch in 16-byte chunks
     for (int64_t idx = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; idx < total;
          idx += (int64_t)gridDim.x * blockDim.x) {
-        const int64_t t = idx / chunks, c = idx % chunks;
-        uint4 v[COMBINE_MAX_K];
-        float g[COMBINE_MAX_K];
-#pragma unroll
-        for (int j = 0; j < COMBINE_MAX_K; ++j) {
-            if (j < k) {
-                int64_t d = __ldg(dest + t * k + j);
-                g[j] = __ldg(w + t * k + j);
-                if (d >= y_rows) {
-                    atomicCAS(status, 0, FP8FG_EDEVICE);
-                    d = -1;
-                }
-                if (d >= 0) {
-                    v[j] = __ldg(reinterpret_cast<const uint4 *>(y + d * ldy) + c);
-                } else {
-                    v[j] = make_uint4(0, 0, 0, 0);
-                    g[j] = 0.0f;  // a skipped slot adds +0, which leaves every sum unchanged
-                }
-            }
-        }
+        const int64_t t = idx / chunks;
+        const uint4 *yc = reinterpret_cast<const uint4 *>(y) + (idx - t * chunks);
+        const int32_t *dt = dest + t * k;
+        const float *wt = w + t * k;
         float acc[8];
 #pragma unroll
         for (int e = 0; e < 8; ++e)
             acc[e] = 0.0f;
+        for (int j0 = 0; j0 < k; j0 += COMBINE_BATCH) {
+            uint4 v[COMBINE_BATCH];
+            unsigned live = 0;  // slots of the batch with a row; the others add nothing
 #pragma unroll
-        for (int j = 0; j < COMBINE_MAX_K; ++j) {
-            if (j < k) {
-                const uint32_t u[4] = {v[j].x, v[j].y, v[j].z, v[j].w};
+            for (int b = 0; b < COMBINE_BATCH; ++b) {
+                v[b] = make_uint4(0, 0, 0, 0);
+                if (j0 + b < k) {
+                    const int64_t d = __ldg(dt + j0 + b);
+                    if (d >= y_rows) {
+                        atomicCAS(status, 0, FP8FG_EDEVICE);
+                    } else if (d >= 0) {
+                        v[b] = __ldg(yc + d * ldy16);
+                        live |= 1u << b;
+                    }
+                }
+            }
 #pragma unroll
-                for (int e = 0; e < 4; ++e) {
-                    acc[2 * e] = __fadd_rn(acc[2 * e], __fmul_rn(g[j], bf16_lo(u[e])));
-                    acc[2 * e + 1] = __fadd_rn(acc[2 * e + 1], __fmul_rn(g[j], bf16_hi(u[e])));
+            for (int b = 0; b < COMBINE_BATCH; ++b) {
+                if (live & (1u << b)) {
+                    const float g = __ldg(wt + j0 + b);
+                    const uint32_t u[4] = {v[b].x, v[b].y, v[b].z, v[b].w};
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        acc[2 * e] = __fadd_rn(acc[2 * e], __fmul_rn(g, bf16_lo(u[e])));
+                        acc[2 * e + 1] = __fadd_rn(acc[2 * e + 1], __fmul_rn(g, bf16_hi(u[e])));
+                    }
                 }
             }
         }
         if constexpr (F32) {
-            float4 *o = reinterpret_cast<float4 *>(static_cast<float *>(out) + t * ldo) + 2 * c;
+            float4 *o = reinterpret_cast<float4 *>(static_cast<float *>(out) + t * ldo) + 2 * (idx - t * chunks);
             o[0] = make_float4(acc[0], acc[1], acc[2], acc[3]);
             o[1] = make_float4(acc[4], acc[5], acc[6], acc[7]);
         } else {
@@ -82,7 +88,7 @@ __global__ void __launch_bounds__(COMBINE_THREADS) moe_combine_kernel(const uint
                 const __nv_bfloat162 h = __floats2bfloat162_rn(acc[2 * e], acc[2 * e + 1]);
                 ow[e] = *reinterpret_cast<const uint32_t *>(&h);
             }
-            reinterpret_cast<uint4 *>(static_cast<uint16_t *>(out) + t * ldo)[c] = o;
+            reinterpret_cast<uint4 *>(static_cast<uint16_t *>(out) + t * ldo)[idx - t * chunks] = o;
         }
     }
 }
@@ -115,7 +121,7 @@ extern "C" int fp8_moe_combine(const void *y, int64_t ldy, int64_t y_rows, const
         return FP8FG_ECUDA;
     const int64_t chunks = N / 8, total = T * chunks;
     const int64_t want = (total + COMBINE_THREADS - 1) / COMBINE_THREADS;
-    const int64_t cap = (int64_t)sm_count() * 8;  // 8 CTAs of 256 per SM; the loop strides past the rest
+    const int64_t cap = (int64_t)sm_count() * COMBINE_CTAS_PER_SM * 4;  // four waves; the loop strides past the rest
     const unsigned grid = (unsigned)(want < cap ? want : (cap > 0 ? cap : 1));
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     if (out_kind == FP8FG_OUT_F32)
