@@ -416,7 +416,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         // MMAs of different blocks are independent (each block starts with
         // accumulate off), and each issuer's commits track its own MMAs.
         setmaxnreg_dec<Regs<MODE>::LOW>();
-        if (lane == 0) {
+        // The whole warp runs the loop and waits (so that the descriptors
+        // are warp-uniform values); one elected lane issues the MMAs and
+        // the commit.
+        {
             constexpr uint32_t IDESC = idesc_e4m3_f32(BM, BN, MODE == DGRAD);
             constexpr int NI = MMA_ISSUERS<MODE>();
             const int issuer = warp - 1;
@@ -435,14 +438,16 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                     // block's phase); the first two blocks find it free
                     if (g >= 2) {
                         const int64_t h = g - 2;
-                        if (!mbar_wait(tempty_bar + 8 * (uint32_t)(h % STAGES), (uint32_t)((h / STAGES) & 1), wc,
-                                       FP8FG_ETIMEOUT)) {
+                        const bool got = mbar_wait(tempty_bar + 8 * (uint32_t)(h % STAGES),
+                                                   (uint32_t)((h / STAGES) & 1), wc, FP8FG_ETIMEOUT);
+                        if (!__all_sync(0xffffffffu, got)) {
                             ok = false;
                             break;
                         }
                     }
                     tc_fence_after();
-                    if (!mbar_wait(full_bar + 8 * stage, phase, wc, FP8FG_ETIMEOUT)) {
+                    const bool got = mbar_wait(full_bar + 8 * stage, phase, wc, FP8FG_ETIMEOUT);
+                    if (!__all_sync(0xffffffffu, got)) {
                         ok = false;
                         break;
                     }
@@ -450,27 +455,30 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                     const uint32_t a_addr = sbase + L::a_off + stage * A_STAGE_BYTES;
                     const uint32_t b_addr = sbase + L::b_off + stage * B_STAGE_BYTES;
                     const uint32_t d = tmem_base + buf * BN;
+                    if (elect_one_sync()) {
 #pragma unroll
-                    for (int k = 0; k < BK / MMA_K; ++k) {
-                        // K-major, 128-byte rows: step K by 32 bytes inside the swizzle atom
-                        const uint64_t adesc = smem_desc_sw128(a_addr + k * MMA_K, 0, 1024);
-                        uint64_t bdesc;
-                        if constexpr (MODE == DGRAD)
-                            // N-major: 32 K-rows = 4 groups of 8 rows (1024 B each);
-                            // the two 128-column halves are 16 KB apart.
-                            bdesc = smem_desc_sw128(b_addr + k * MMA_K * 128, B_STAGE_BYTES / 2, 1024);
-                        else
-                            bdesc = smem_desc_sw128(b_addr + k * MMA_K, 0, 1024);
-                        mma_f8f6f4(d, adesc, bdesc, IDESC, k > 0 ? 1u : 0u);
+                        for (int k = 0; k < BK / MMA_K; ++k) {
+                            // K-major, 128-byte rows: step K by 32 bytes inside the swizzle atom
+                            const uint64_t adesc = smem_desc_sw128(a_addr + k * MMA_K, 0, 1024);
+                            uint64_t bdesc;
+                            if constexpr (MODE == DGRAD)
+                                // N-major: 32 K-rows = 4 groups of 8 rows (1024 B each);
+                                // the two 128-column halves are 16 KB apart.
+                                bdesc = smem_desc_sw128(b_addr + k * MMA_K * 128, B_STAGE_BYTES / 2, 1024);
+                            else
+                                bdesc = smem_desc_sw128(b_addr + k * MMA_K, 0, 1024);
+                            mma_f8f6f4(d, adesc, bdesc, IDESC, k > 0 ? 1u : 0u);
+                        }
+                        mma_commit(tfull_bar + 8 * buf);
                     }
-                    mma_commit(tfull_bar + 8 * buf);
+                    __syncwarp();
                     committed = 1;
                     last_buf = buf;
                     last_par = tphase;
                 }
             }
-            if (!ok && committed) {
-                // drain: the last commit covers every MMA this thread issued before it
+            if (!ok && committed && lane == 0) {
+                // drain: the last commit covers every MMA this warp issued before it
                 const uint32_t bar = tfull_bar + 8 * last_buf;
                 const uint64_t t0 = global_timer_ns();
                 while (!mbar_try_wait(bar, last_par) && global_timer_ns() - t0 < p.wait_limit_ns) {
