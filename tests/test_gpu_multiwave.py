@@ -11,7 +11,9 @@ compare every output element with the oracle:
 - fprop, dgrad and wgrad at about 3x the SM count in 128x256 tiles with
   three contraction blocks;
 - the grouped MoE GEMM (row-index and expert-order forms) with more than
-  400 tiles over experts of 0..400 rows;
+  400 tiles over experts of 0..400 rows; with 100 experts all inside one
+  128-row tile (500 tiles); and with 2100 experts, 40 of them routed (some
+  past expert 2047);
 - the whole dense projection workload (4096 x 7168 x 7168, bf16 out), all
   rows;
 - the full-size training trio quantised by the dual-output quantiser, as
@@ -149,6 +151,64 @@ def test_grouped_multiwave(form):
         assert np.array_equal(wo[e], qe) and np.array_equal(swo[e], se)
     c, _, t = oracle.grouped(xo, sxo, row_index, off, wo, swo)
     check_gemm(to_np(y), c, t, False, "grouped multiwave (%s)" % form)
+
+
+def _grouped_against_oracle(x, w, row_index, off, form, what):
+    R = int(off[-1])
+    wq, sw = fg.fp8_quant_128x128(w)
+    of = torch.from_numpy(off).to(DEV)
+    ri = torch.from_numpy(row_index).to(DEV)
+    if form == "row_index":
+        xq, sx = fg.fp8_quant_1x128(x)
+        y = fg.fp8_grouped_gemm(xq, sx, ri, of, wq, sw, n_rows=R, out_dtype=torch.float32)
+    else:
+        xq, sx = fg.fp8_quant_1x128_gather(x, ri)
+        y = fg.fp8_grouped_gemm(xq, sx, None, of, wq, sw, n_rows=R, out_dtype=torch.float32)
+    assert fg.device_status() == 0
+    xo, sxo = oracle.quant_1x128(bits(x))
+    wo, swo = to_np(wq), to_np(sw)
+    for e in np.flatnonzero(np.diff(off))[:3]:
+        qe, se = oracle.quant_128x128(bits(w[int(e)]))
+        assert np.array_equal(wo[e], qe) and np.array_equal(swo[e], se)
+    c, _, t = oracle.grouped(xo, sxo, row_index, off, wo, swo)
+    check_gemm(to_np(y), c, t, False, what)
+
+
+def _routing(rng, T, counts):
+    row_index = np.concatenate([np.sort(rng.choice(T, c, replace=False)) if c else np.zeros(0, np.int64)
+                                for c in counts]).astype(np.int32)
+    return row_index, np.concatenate([[0], np.cumsum(counts)]).astype(np.int32)
+
+
+@pytest.mark.parametrize("form", ["row_index", "expert_order"])
+def test_grouped_multiwave_single_class(form):
+    """100 experts of 1..128 rows: every expert is one m-tile."""
+    E, T, K, N = 100, 1000, 384, 1280
+    g = _gen(41)
+    x = torch.randn(T, K, generator=g, device=DEV).to(torch.bfloat16)
+    w = (torch.randn(E, N, K, generator=g, device=DEV) * 0.02).to(torch.bfloat16)
+    rng = np.random.default_rng(41)
+    counts = rng.integers(1, 129, E)
+    counts[[0, 1]] = [1, 128]
+    row_index, off = _routing(rng, T, counts)
+    assert E * (N // 256) >= 400
+    _grouped_against_oracle(x, w, row_index, off, form, "grouped, one-m-tile experts (%s)" % form)
+
+
+@pytest.mark.parametrize("form", ["row_index", "expert_order"])
+def test_grouped_many_experts_plain_order(form):
+    """2100 experts, 40 of them routed, some past expert 2047."""
+    E, T, K, N = 2100, 1000, 384, 256
+    g = _gen(42)
+    x = torch.randn(T, K, generator=g, device=DEV).to(torch.bfloat16)
+    w = (torch.randn(E, N, K, generator=g, device=DEV) * 0.02).to(torch.bfloat16)
+    rng = np.random.default_rng(42)
+    counts = np.zeros(E, np.int64)
+    used = np.concatenate([rng.choice(2048, 30, replace=False), 2048 + rng.choice(E - 2048, 10, replace=False)])
+    counts[used] = rng.integers(1, 400, used.size)
+    counts[E - 1] = 129
+    row_index, off = _routing(rng, T, counts)
+    _grouped_against_oracle(x, w, row_index, off, form, "grouped, 2100 experts (%s)" % form)
 
 
 def test_dense_config_every_element():
