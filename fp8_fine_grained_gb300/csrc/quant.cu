@@ -18,6 +18,7 @@
 #include "group_rule.cuh"
 #include "host_common.h"
 #include "ptx.cuh"
+#include "tensor_map.h"
 
 namespace fp8fg {
 namespace {
@@ -33,12 +34,22 @@ __device__ __forceinline__ uint32_t absmax_bits8(const uint4 &v)
     return max(m & 0xFFFFu, m >> 16);
 }
 
+// two bf16 values (the halves of w) times inv as one packed pair of FP32
+// products (each an IEEE round-to-nearest product, as __fmul_rn) -> two
+// E4M3 bytes
+__device__ __forceinline__ uint32_t quant2x(uint32_t w, float2 inv2)
+{
+    const float2 p = __fmul2_rn(make_float2(bf16_lo(w), bf16_hi(w)), inv2);
+    return cvt_e4m3x2(p.x, p.y);
+}
+
 // 8 bf16 -> 8 E4M3 bytes
 __device__ __forceinline__ uint2 quant8(const uint4 &v, float inv)
 {
+    const float2 inv2 = make_float2(inv, inv);
     uint2 o;
-    o.x = quant2(v.x, inv) | (quant2(v.y, inv) << 16);
-    o.y = quant2(v.z, inv) | (quant2(v.w, inv) << 16);
+    o.x = quant2x(v.x, inv2) | (quant2x(v.y, inv2) << 16);
+    o.y = quant2x(v.z, inv2) | (quant2x(v.w, inv2) << 16);
     return o;
 }
 
@@ -316,83 +327,166 @@ __global__ void __launch_bounds__(256, 8) quant_cols_t_kernel(const uint16_t *__
 // --------------------------------------- 1x128 and 128x1 from one read ----
 // Both activation layouts a training step needs (row groups for fprop and
 // dgrad, column groups transposed for wgrad) from a single read of x: the
-// CTA holds a 128x128 tile, quantises its rows straight from registers and
-// its columns from a shared-memory copy. The outputs are bit-identical to
-// fp8_quant_1x128 with transpose 0 and 1 (same group rule, same products).
-// 4.06 bytes of traffic per element instead of 2 x 3.03.
+// CTA quantises a 128x128 tile's rows and its columns from one
+// shared-memory copy. The outputs are bit-identical to fp8_quant_1x128
+// with transpose 0 and 1 (same group rule, same products). 4.06 bytes of
+// traffic per element instead of 2 x 3.03.
+//
+// Persistent, three CTAs per SM: each CTA walks its tiles with a stride of
+// the grid and has the next tile's 32 KB brought in by TMA (into the other
+// of two buffers) while it quantises the current one, so every SM keeps
+// loads in flight through the compute phases. The wait on a tile is bounded
+// (FP8FG_ETIMEOUT in the status word, then the CTA drains and leaves).
+constexpr int DUAL_CTAS_PER_SM = 3;
+constexpr uint32_t DUAL_TILE_BYTES = GROUP * GROUP * 2;
+
+struct DualSmem {
+    uint16_t tile[2][GROUP][GROUP];  // two bf16 tiles, rows of 256 bytes (the TMA box as it lands)
+    uint64_t bar[2];                 // "tile landed", one per buffer
+    uint32_t s_cmax[4][GROUP / 2];   // column-pair maxima (two 16-bit magnitudes) of each row quarter
+    float s_cinv[GROUP];             // the columns' 448/amax
+    float s_row[GROUP];
+    int abort;
+};
+
 template <bool P2>
-__global__ void __launch_bounds__(256, 5) quant_dual_kernel(const uint16_t *__restrict__ x, int64_t ldx,
-                                                            uint8_t *__restrict__ q, int64_t ldq,
-                                                            float *__restrict__ scales, int64_t ld_s,
-                                                            uint8_t *__restrict__ qT, int64_t ldqT,
-                                                            float *__restrict__ scalesT, int64_t ld_sT)
+__global__ void __launch_bounds__(256, DUAL_CTAS_PER_SM)
+    quant_dual_kernel(const __grid_constant__ CUtensorMap tmx, int64_t tiles_c, int64_t n_tiles,
+                      uint8_t *__restrict__ q, int64_t ldq, float *__restrict__ scales, int64_t ld_s,
+                      uint8_t *__restrict__ qT, int64_t ldqT, float *__restrict__ scalesT, int64_t ld_sT, int *status,
+                      uint64_t wait_limit_ns)
 {
     griddep_launch_dependents();  // a dependent GEMM may set itself up under this grid's tail
-    __shared__ __align__(16) uint16_t tile[GROUP][GROUP];
-    __shared__ uint32_t s_amax[2][GROUP];
-    __shared__ float s_row[GROUP];
+    extern __shared__ __align__(128) uint8_t dual_raw[];
+    DualSmem &S = *reinterpret_cast<DualSmem *>(dual_raw);
     const int tid = threadIdx.x;
     const int l = tid & 15;
-    const int64_t c0 = (int64_t)blockIdx.x * GROUP;
-    const int64_t r0 = (int64_t)blockIdx.y * GROUP;
-
-    // chunk i*256 + tid = row (i*16 + tid/16), columns (tid%16)*8 .. +7
-    uint4 v[8];
-#pragma unroll
-    for (int i = 0; i < 8; ++i)
-        v[i] = ld_stream_v4(x + (r0 + i * 16 + (tid >> 4)) * ldx + c0 + l * 8);
-    // row groups: one half-warp per row, the eight rows' scales in one batch
-    uint32_t mr[8];
-#pragma unroll
-    for (int i = 0; i < 8; ++i) {
-        const int rr = i * 16 + (tid >> 4);
-        *reinterpret_cast<uint4 *>(&tile[rr][l * 8]) = v[i];
-        mr[i] = absmax_bits8(v[i]);
-#pragma unroll
-        for (int off = 8; off >= 1; off >>= 1)
-            mr[i] = max(mr[i], __shfl_xor_sync(0xffffffffu, mr[i], off));
-    }
-    float sr[8], ir[8];
-    group_scales_batched<8, P2>(mr, sr, ir);
-#pragma unroll
-    for (int i = 0; i < 8; ++i) {
-        const int rr = i * 16 + (tid >> 4);
-        *reinterpret_cast<uint2 *>(q + (r0 + rr) * ldq + c0 + l * 8) = quant8(v[i], ir[i]);
-        if (l == 0)
-            s_row[rr] = sr[i];
+    const uint32_t bar0 = smem_u32(&S.bar[0]);
+    if (tid == 0) {
+        mbar_init(bar0, 1);
+        mbar_init(bar0 + 8, 1);
+        S.abort = 0;
+        fence_mbar_init();
+        tma_prefetch_desc(&tmx);
     }
     __syncthreads();
-    if (tid < GROUP)
-        scales[(c0 / GROUP) * ld_s + r0 + tid] = s_row[tid];
-
-    // column groups: thread (c, part) covers rows part*64 .. +63 of column c
-    const int c = tid & (GROUP - 1), part = tid >> 7;
-    uint32_t m = 0;
-#pragma unroll 8
-    for (int i = 0; i < 64; ++i)
-        m = max(m, (uint32_t)(tile[part * 64 + i][c] & 0x7FFFu));
-    s_amax[part][c] = m;
-    __syncthreads();
-    m = max(s_amax[0][c], s_amax[1][c]);
-    const ScalePair sp = group_scale_rule<P2>(__uint_as_float(m << 16));
-    const int64_t col = c0 + c;
-    uint4 *dst = reinterpret_cast<uint4 *>(qT + col * ldqT + r0 + part * 64);
-#pragma unroll
-    for (int h = 0; h < 4; ++h) {
-        uint32_t packed[4];
-#pragma unroll
-        for (int j = 0; j < 4; ++j) {
-            const int rb = part * 64 + h * 16 + j * 4;
-            const uint32_t lo = cvt_e4m3x2(__fmul_rn(__uint_as_float((uint32_t)tile[rb + 0][c] << 16), sp.inv),
-                                           __fmul_rn(__uint_as_float((uint32_t)tile[rb + 1][c] << 16), sp.inv));
-            const uint32_t hi = cvt_e4m3x2(__fmul_rn(__uint_as_float((uint32_t)tile[rb + 2][c] << 16), sp.inv),
-                                           __fmul_rn(__uint_as_float((uint32_t)tile[rb + 3][c] << 16), sp.inv));
-            packed[j] = lo | (hi << 16);
+    const WaitCtl wc{&S.abort, status, wait_limit_ns};
+    auto fetch = [&](int64_t t, uint32_t b) {
+        mbar_arrive_expect_tx(bar0 + 8 * b, DUAL_TILE_BYTES);
+        tma_load_2d(smem_u32(&S.tile[b][0][0]), &tmx, (int32_t)((t % tiles_c) * GROUP),
+                    (int32_t)((t / tiles_c) * GROUP), bar0 + 8 * b);
+    };
+    if (tid == 0 && (int64_t)blockIdx.x < n_tiles)
+        fetch(blockIdx.x, 0);
+    uint32_t it = 0;
+    for (int64_t t = blockIdx.x; t < n_tiles; t += gridDim.x, ++it) {
+        const uint32_t b = it & 1;
+        // the other buffer was last read in the previous iteration, which
+        // ended at a barrier: it may be refilled
+        const bool ahead = t + gridDim.x < n_tiles;
+        if (tid == 0 && ahead)
+            fetch(t + gridDim.x, b ^ 1);
+        const bool got = mbar_wait(bar0 + 8 * b, (it >> 1) & 1, wc, FP8FG_ETIMEOUT);
+        if (!__syncthreads_and(got)) {
+            // drain the copies this CTA still has in flight before leaving
+            if (tid == 0) {
+                const uint64_t t0 = global_timer_ns();
+                while (!mbar_try_wait(bar0 + 8 * b, (it >> 1) & 1) && global_timer_ns() - t0 < wait_limit_ns) {
+                }
+                while (ahead && !mbar_try_wait(bar0 + 8 * (b ^ 1), ((it + 1) >> 1) & 1) &&
+                       global_timer_ns() - t0 < 2 * wait_limit_ns) {
+                }
+            }
+            return;
         }
-        dst[h] = make_uint4(packed[0], packed[1], packed[2], packed[3]);
+        uint16_t(*tile)[GROUP] = S.tile[b];
+        const int64_t c0 = (t % tiles_c) * GROUP, r0 = (t / tiles_c) * GROUP;
+
+        // row groups: chunk i*256 + tid = row (i*16 + tid/16), columns
+        // (tid%16)*8 .. +7; one half-warp per row, the eight rows' scales
+        // in one batch
+        uint4 v[8];
+        uint32_t mr[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            v[i] = *reinterpret_cast<const uint4 *>(&tile[i * 16 + (tid >> 4)][l * 8]);
+            mr[i] = absmax_bits8(v[i]);
+        }
+        // half-warp maxima, two rows' 16-bit magnitudes per shuffle
+#pragma unroll
+        for (int i = 0; i < 8; i += 2) {
+            uint32_t m2 = mr[i] | (mr[i + 1] << 16);
+#pragma unroll
+            for (int off = 8; off >= 1; off >>= 1)
+                m2 = __vmaxu2(m2, __shfl_xor_sync(0xffffffffu, m2, off));
+            mr[i] = m2 & 0xFFFFu;
+            mr[i + 1] = m2 >> 16;
+        }
+        float sr[8], ir[8];
+        group_scales_batched<8, P2>(mr, sr, ir);
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            const int rr = i * 16 + (tid >> 4);
+            *reinterpret_cast<uint2 *>(q + (r0 + rr) * ldq + c0 + l * 8) = quant8(v[i], ir[i]);
+            if (l == 0)
+                S.s_row[rr] = sr[i];
+        }
+
+        // column groups: thread (cp, part) covers the column pair 2cp, 2cp+1
+        // over rows part*32 .. +31, reading both columns as one 32-bit word
+        // (a warp reads 128 contiguous bytes of a row)
+        const int cp = tid & (GROUP / 2 - 1), part = tid >> 6;
+        const uint32_t *t32 = reinterpret_cast<const uint32_t *>(&tile[0][0]);
+        uint32_t m2 = 0;
+#pragma unroll 8
+        for (int i = 0; i < 32; ++i)
+            m2 = __vmaxu2(m2, t32[(part * 32 + i) * (GROUP / 2) + cp] & 0x7FFF7FFFu);
+        S.s_cmax[part][cp] = m2;
+        __syncthreads();
+        if (tid < GROUP) {
+            // column tid: its group's scale pair, once per column
+            scales[(c0 / GROUP) * ld_s + r0 + tid] = S.s_row[tid];
+            uint32_t m = 0;
+#pragma unroll
+            for (int pq = 0; pq < 4; ++pq) {
+                const uint32_t w = S.s_cmax[pq][tid >> 1];
+                m = max(m, (tid & 1) ? (w >> 16) : (w & 0xFFFFu));
+            }
+            const ScalePair sp = group_scale_rule<P2>(__uint_as_float(m << 16));
+            S.s_cinv[tid] = sp.inv;
+            scalesT[(r0 / GROUP) * ld_sT + c0 + tid] = sp.s;
+        }
+        __syncthreads();
+        // codes: rows r, r+1 of one column form one packed product and one
+        // E4M3 pair; each column's 32 codes go out as one 32-byte run
+        const float2 inva = make_float2(S.s_cinv[2 * cp], S.s_cinv[2 * cp]);
+        const float2 invb = make_float2(S.s_cinv[2 * cp + 1], S.s_cinv[2 * cp + 1]);
+        uint32_t pa[8], pb[8];
+#pragma unroll
+        for (int rp = 0; rp < 16; ++rp) {
+            const uint32_t w0 = t32[(part * 32 + 2 * rp) * (GROUP / 2) + cp];
+            const uint32_t w1 = t32[(part * 32 + 2 * rp + 1) * (GROUP / 2) + cp];
+            const float2 xa = __fmul2_rn(make_float2(bf16_lo(w0), bf16_lo(w1)), inva);
+            const float2 xb = __fmul2_rn(make_float2(bf16_hi(w0), bf16_hi(w1)), invb);
+            const uint32_t ca = cvt_e4m3x2(xa.x, xa.y), cb = cvt_e4m3x2(xb.x, xb.y);
+            if (rp & 1) {
+                pa[rp >> 1] |= ca << 16;
+                pb[rp >> 1] |= cb << 16;
+            } else {
+                pa[rp >> 1] = ca;
+                pb[rp >> 1] = cb;
+            }
+        }
+        uint4 *da = reinterpret_cast<uint4 *>(qT + (c0 + 2 * cp) * ldqT + r0 + part * 32);
+        uint4 *db = reinterpret_cast<uint4 *>(qT + (c0 + 2 * cp + 1) * ldqT + r0 + part * 32);
+        da[0] = make_uint4(pa[0], pa[1], pa[2], pa[3]);
+        da[1] = make_uint4(pa[4], pa[5], pa[6], pa[7]);
+        db[0] = make_uint4(pb[0], pb[1], pb[2], pb[3]);
+        db[1] = make_uint4(pb[4], pb[5], pb[6], pb[7]);
+        // every read of this buffer and of s_row / s_cmax / s_cinv is done
+        // before the next iteration refills the other buffer and rewrites them
+        __syncthreads();
     }
-    if (part == 0)
-        scalesT[(r0 / GROUP) * ld_sT + col] = sp.s;
 }
 
 // ------------------------------------------------------- 128x128 blocks ----
@@ -562,11 +656,22 @@ int quant_1x128_dual(const void *x, int64_t rows, int64_t cols, int64_t ldx, uin
         return FP8FG_EALIGN;
     if (!device_supported())
         return FP8FG_EUNSUPPORTED;
-    const int64_t gx = cols / GROUP, gy = rows / GROUP;
-    if (gx > 0x7FFFFFFF || gy > 65535)
+    const int64_t tiles_c = cols / GROUP, n_tiles = tiles_c * (rows / GROUP);
+    if (n_tiles > 0x7FFFFFFF)
         return FP8FG_EINVAL;
-    quant_dual_kernel<P2><<<dim3((unsigned)gx, (unsigned)gy), 256, 0, static_cast<cudaStream_t>(stream)>>>(
-        static_cast<const uint16_t *>(x), ldx, q, ldq, scales, ld_s, qT, ldqT, scalesT, ld_sT);
+    int *status = status_word_ptr();
+    CUtensorMap tmx;
+    if (!status || !make_map_bf16_tile(&tmx, x, (uint64_t)cols, (uint64_t)rows, (uint64_t)ldx, GROUP, GROUP))
+        return FP8FG_ECUDA;
+    auto k = quant_dual_kernel<P2>;
+    if (cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sizeof(DualSmem)) != cudaSuccess) {
+        cudaGetLastError();
+        return FP8FG_ECUDA;
+    }
+    const int64_t cap = (int64_t)sm_count() * DUAL_CTAS_PER_SM;
+    const unsigned grid = (unsigned)(n_tiles < cap ? n_tiles : (cap > 0 ? cap : 1));
+    k<<<grid, 256, sizeof(DualSmem), static_cast<cudaStream_t>(stream)>>>(
+        tmx, tiles_c, n_tiles, q, ldq, scales, ld_s, qT, ldqT, scalesT, ld_sT, status, wait_limit_ns());
     return launch_status();
 }
 

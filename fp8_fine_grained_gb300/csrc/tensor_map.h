@@ -1,4 +1,4 @@
-// Host-side TMA tensor-map helpers shared by the GEMM translation units.
+// Host-side TMA tensor-map helpers shared by the library's translation units.
 #pragma once
 
 #include <cuda.h>
@@ -61,6 +61,24 @@ inline bool make_map_f32_row(CUtensorMap *m, const void *base, uint64_t cols, ui
     cuuint32_t estr[2] = {1, 1};
     return fn(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, const_cast<void *>(base), dims, strides, box, estr,
               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_NONE,
+              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// 2-D bf16 tensor [rows][cols] with row pitch `ld` elements; box
+// box_cols x box_rows landing as plain rows (no swizzle). Out-of-range box
+// elements read 0.
+inline bool make_map_bf16_tile(CUtensorMap *m, const void *base, uint64_t cols, uint64_t rows, uint64_t ld,
+                               uint32_t box_cols, uint32_t box_rows)
+{
+    EncodeTiledFn fn = encode_fn();
+    if (!fn)
+        return false;
+    cuuint64_t dims[2] = {cols, rows};
+    cuuint64_t strides[1] = {ld * 2};
+    cuuint32_t box[2] = {box_cols, box_rows};
+    cuuint32_t estr[2] = {1, 1};
+    return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(base), dims, strides, box, estr,
+              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
