@@ -273,7 +273,8 @@ __global__ void __launch_bounds__(256, 8) quant_cols_t_kernel(const uint16_t *__
 {
     griddep_launch_dependents();  // a dependent GEMM may set itself up under this grid's tail
     __shared__ __align__(16) uint16_t tile[GROUP][QT_COLS];
-    __shared__ uint32_t s_amax[4][QT_COLS];
+    __shared__ uint32_t s_cmax[8][QT_COLS / 2];  // column-pair maxima of each 16-row part
+    __shared__ float s_inv[QT_COLS];
     const int tid = threadIdx.x;
     const int64_t c0 = (int64_t)blockIdx.x * QT_COLS;
     const int64_t r0 = (int64_t)blockIdx.y * GROUP;
@@ -295,32 +296,57 @@ __global__ void __launch_bounds__(256, 8) quant_cols_t_kernel(const uint16_t *__
     }
     __syncthreads();
 
-    const int c = tid & (QT_COLS - 1), part = tid >> 6;
-    uint32_t m = 0;
-#pragma unroll 8
-    for (int i = 0; i < 32; ++i)
-        m = max(m, (uint32_t)(tile[part * 32 + i][c] & 0x7FFFu));
-    s_amax[part][c] = m;
-    __syncthreads();
-    m = max(max(s_amax[0][c], s_amax[1][c]), max(s_amax[2][c], s_amax[3][c]));
-    const ScalePair sp = group_scale_rule<P2>(__uint_as_float(m << 16));
-    const int64_t col = c0 + c;
-    if (col < cols) {
-        uint32_t packed[8];
+    // thread (cp, part): the column pair 2cp, 2cp+1 over rows part*16 ..
+    // +15, both columns read as one 32-bit word (a warp reads one 128-byte
+    // row) and reduced with packed 16-bit maxima
+    const int cp = tid & (QT_COLS / 2 - 1), part = tid >> 5;
+    const uint32_t *t32 = reinterpret_cast<const uint32_t *>(&tile[0][0]);
+    uint32_t m2 = 0;
 #pragma unroll
-        for (int j = 0; j < 8; ++j) {
-            const int rb = part * 32 + j * 4;
-            const uint32_t lo = cvt_e4m3x2(__fmul_rn(__uint_as_float((uint32_t)tile[rb + 0][c] << 16), sp.inv),
-                                           __fmul_rn(__uint_as_float((uint32_t)tile[rb + 1][c] << 16), sp.inv));
-            const uint32_t hi = cvt_e4m3x2(__fmul_rn(__uint_as_float((uint32_t)tile[rb + 2][c] << 16), sp.inv),
-                                           __fmul_rn(__uint_as_float((uint32_t)tile[rb + 3][c] << 16), sp.inv));
-            packed[j] = lo | (hi << 16);
+    for (int i = 0; i < 16; ++i)
+        m2 = __vmaxu2(m2, t32[(part * 16 + i) * (QT_COLS / 2) + cp] & 0x7FFF7FFFu);
+    s_cmax[part][cp] = m2;
+    __syncthreads();
+    if (tid < QT_COLS) {
+        // column tid: the group's scale pair, once per column
+        uint32_t m = 0;
+#pragma unroll
+        for (int pq = 0; pq < 8; ++pq) {
+            const uint32_t w = s_cmax[pq][tid >> 1];
+            m = max(m, (tid & 1) ? (w >> 16) : (w & 0xFFFFu));
         }
-        uint4 *dst = reinterpret_cast<uint4 *>(qT + col * ldq + r0 + part * 32);
-        dst[0] = make_uint4(packed[0], packed[1], packed[2], packed[3]);
-        dst[1] = make_uint4(packed[4], packed[5], packed[6], packed[7]);
-        if (part == 0)
-            scales[(r0 / GROUP) * ld_s + col] = sp.s;
+        const ScalePair sp = group_scale_rule<P2>(__uint_as_float(m << 16));
+        s_inv[tid] = sp.inv;
+        if (c0 + tid < cols)
+            scales[(r0 / GROUP) * ld_s + c0 + tid] = sp.s;
+    }
+    __syncthreads();
+    // codes: rows r, r+1 of one column form one packed product and one
+    // E4M3 pair; each column's 16 codes go out as one 16-byte piece of its
+    // transposed row
+    const int64_t col = c0 + 2 * cp;
+    if (col < cols) {
+        const float2 inva = make_float2(s_inv[2 * cp], s_inv[2 * cp]);
+        const float2 invb = make_float2(s_inv[2 * cp + 1], s_inv[2 * cp + 1]);
+        uint32_t pa[4], pb[4];
+#pragma unroll
+        for (int rp = 0; rp < 8; ++rp) {
+            const uint32_t w0 = t32[(part * 16 + 2 * rp) * (QT_COLS / 2) + cp];
+            const uint32_t w1 = t32[(part * 16 + 2 * rp + 1) * (QT_COLS / 2) + cp];
+            const float2 xa = __fmul2_rn(make_float2(bf16_lo(w0), bf16_lo(w1)), inva);
+            const float2 xb = __fmul2_rn(make_float2(bf16_hi(w0), bf16_hi(w1)), invb);
+            const uint32_t ca = cvt_e4m3x2(xa.x, xa.y), cb = cvt_e4m3x2(xb.x, xb.y);
+            if (rp & 1) {
+                pa[rp >> 1] |= ca << 16;
+                pb[rp >> 1] |= cb << 16;
+            } else {
+                pa[rp >> 1] = ca;
+                pb[rp >> 1] = cb;
+            }
+        }
+        *reinterpret_cast<uint4 *>(qT + col * ldq + r0 + part * 16) = make_uint4(pa[0], pa[1], pa[2], pa[3]);
+        if (col + 1 < cols)
+            *reinterpret_cast<uint4 *>(qT + (col + 1) * ldq + r0 + part * 16) = make_uint4(pb[0], pb[1], pb[2], pb[3]);
     }
 }
 
