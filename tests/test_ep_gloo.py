@@ -22,8 +22,10 @@ from fp8_fine_grained_gb300 import ep
 E, K, N, T, TOPK = 8, 256, 256, 20, 3
 
 
-def _problem(rank):
-    """Experts (same on every rank) and this rank's tokens and routing."""
+def _problem(rank, skewed=False):
+    """Experts (same on every rank) and this rank's tokens and routing.
+    skewed: rank 1 routes every token to its own experts (it sends rank 0
+    nothing) and rank 0's token 7 uses no slot at all."""
     g = torch.Generator().manual_seed(1234)
     w = (torch.randn(E, N, K, generator=g) * 0.02).to(torch.bfloat16)
     wq, sw = [], []
@@ -34,8 +36,12 @@ def _problem(rank):
     gt = torch.Generator().manual_seed(100 + rank)
     x = (torch.randn(T, K, generator=gt) * torch.exp(torch.randn(K, generator=gt))).to(torch.bfloat16)
     logits = torch.randn(T, E, generator=gt)
+    if skewed and rank == 1:
+        logits[:, :E // 2] = -1e9                       # only experts E/2.. (rank 1's own)
     topk = torch.topk(logits, TOPK, dim=1).indices.to(torch.int32)
     topk[3, 1] = -1                                     # one unused slot
+    if skewed and rank == 0:
+        topk[7, :] = -1                                 # a token routed nowhere
     gate = torch.softmax(torch.gather(logits, 1, topk.clamp(min=0).long()), dim=1).to(torch.float32)
     return np.stack(wq), np.stack(sw), x.view(torch.int16).numpy().view(np.uint16), topk, gate
 
@@ -60,12 +66,12 @@ def _reference(wq, sw, xb, topk, gate):
     return oracle.moe_combine(np.stack(rows), dest, gate.numpy())
 
 
-def _rank(rank, world, port, out):
+def _rank(rank, world, port, out, skewed=False):
     import torch.distributed as dist
     os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port), RANK=str(rank), WORLD_SIZE=str(world))
     dist.init_process_group("gloo", rank=rank, world_size=world)
     try:
-        wq, sw, xb, topk, gate = _problem(rank)
+        wq, sw, xb, topk, gate = _problem(rank, skewed)
         Er = E // world
         plan = ep.plan_dispatch(topk, E, world)
         # dispatch: every token quantised once, its codes and scales copied to its k send rows
@@ -101,25 +107,39 @@ def _rank(rank, world, port, out):
             "recv_rows_sorted_by_expert": bool(np.all(np.diff(off) >= 0)),
             "q_recv": q_recv, "s_recv": s_recv, "recv_counts": recv_counts.numpy(),
             "q": q, "s": s, "plan_dest": plan.dest.numpy(), "send_counts": plan.send_counts.numpy(),
+            "out": got,
         }
     finally:
         dist.destroy_process_group()
 
 
-@pytest.fixture(scope="module")
-def two_ranks():
+def _run_two(port, skewed):
     oracle.build.build()
     ctx = mp.get_context("spawn")
     mgr = ctx.Manager()
     out = mgr.dict()
-    port = 29500 + (os.getpid() % 1000)
-    procs = [ctx.Process(target=_rank, args=(r, 2, port, out)) for r in range(2)]
+    procs = [ctx.Process(target=_rank, args=(r, 2, port, out, skewed)) for r in range(2)]
     for p in procs:
         p.start()
     for p in procs:
         p.join(120)
         assert p.exitcode == 0
     return dict(out)
+
+
+@pytest.fixture(scope="module")
+def two_ranks():
+    return _run_two(29500 + (os.getpid() % 1000), False)
+
+
+def test_empty_splits_and_a_token_routed_nowhere():
+    """Rank 1 sends rank 0 no row (zero-size splits in the all-to-alls) and
+    rank 0 has a token whose slots are all unused (its output is zero)."""
+    res = _run_two(30600 + (os.getpid() % 1000), True)
+    assert res[1]["sent"][0] == 0 and res[0]["received"][1] == 0
+    for r in range(2):
+        assert res[r]["combine_equal"], "rank %d" % r
+    assert np.all(res[0]["out"][7] == 0)
 
 
 def test_every_token_output_matches_the_single_process_layer(two_ranks):
