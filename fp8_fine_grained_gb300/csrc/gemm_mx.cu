@@ -113,15 +113,17 @@ struct SmemLayout {
 };
 static_assert(SmemLayout::total <= 232448, "shared memory budget");
 
-// Dense modes: bands of 16 m-tiles, m fastest inside a band (A and B tiles
-// of CTAs that run together stay in L2). Grouped: the experts' tiles.
+// Dense modes: bands of m-tiles, m fastest inside a band (A and B tiles of
+// CTAs that run together stay in L2): 32 m-tiles per band, 16 for the data
+// gradient, whose long contraction makes its panels too large for a band of
+// 32 to stay in L2 (as in the promoted kernel). Grouped: the experts' tiles.
 template <int MODE>
 __device__ __forceinline__ GroupTile decode_tile(int64_t t, const Params &p, const int32_t *prefix)
 {
     if constexpr (MODE == GROUPED_C) {
         return decode_group_tile(t, prefix, p.expert_offsets, p.n_experts, p.n_rows, BM, BN);
     } else {
-        constexpr int64_t BAND = 16;
+        constexpr int64_t BAND = MODE == DGRAD ? 16 : 32;
         const int64_t per_band = BAND * p.num_n_tiles;
         const int64_t band = t / per_band, r = t % per_band;
         const int64_t mfirst = band * BAND;
