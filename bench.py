@@ -108,14 +108,64 @@ def reduce_max(values, pg):
     return [float(v) for v in t.tolist()]
 
 
+class _NvmlClocks:
+    """Read-only NVML queries through the driver's library (ctypes): the SM
+    clock, its maximum, the power draw and the clock event reasons of one
+    GPU. Unavailable (ok False) where the library cannot be loaded."""
+
+    SM = 1  # NVML_CLOCK_SM
+    REASONS = {0x4: "sw_power_cap", 0x8: "hw_slowdown", 0x20: "sw_thermal_slowdown", 0x40: "hw_thermal_slowdown"}
+
+    def __init__(self, index):
+        import ctypes
+        self.ct = ctypes
+        self.ok = False
+        try:
+            self.lib = ctypes.CDLL("libnvidia-ml.so.1")
+            if self.lib.nvmlInit_v2() != 0:
+                return
+            self.h = ctypes.c_void_p()
+            if self.lib.nvmlDeviceGetHandleByIndex_v2(ctypes.c_uint(index), ctypes.byref(self.h)) != 0:
+                return
+            self.reasons_fn = getattr(self.lib, "nvmlDeviceGetCurrentClocksEventReasons", None) or \
+                self.lib.nvmlDeviceGetCurrentClocksThrottleReasons
+            mx = ctypes.c_uint()
+            if self.lib.nvmlDeviceGetMaxClockInfo(self.h, self.SM, ctypes.byref(mx)) != 0:
+                return
+            self.max_mhz = mx.value
+            self.ok = self.sample() is not None
+        except (OSError, AttributeError):
+            self.ok = False
+
+    def sample(self):
+        ct = self.ct
+        clk, mw, rs = ct.c_uint(), ct.c_uint(), ct.c_ulonglong()
+        if self.lib.nvmlDeviceGetClockInfo(self.h, self.SM, ct.byref(clk)) != 0:
+            return None
+        if self.reasons_fn(self.h, ct.byref(rs)) != 0:
+            return None
+        if self.lib.nvmlDeviceGetPowerUsage(self.h, ct.byref(mw)) != 0:
+            mw.value = 0
+        return clk.value, mw.value / 1000.0, rs.value
+
+    def close(self):
+        try:
+            self.lib.nvmlShutdown()
+        except (OSError, AttributeError):
+            pass
+
+
 class ClockSampler:
-    """nvidia-smi clock/throttle sampling (every 50 ms, each sample with its
-    timestamp) around the timed region; the summary keeps only the samples
-    taken inside it."""
+    """Clock and throttle-reason sampling around the timed region, each
+    sample with its timestamp; the summary keeps only the samples taken
+    inside it. Samples come from NVML every millisecond (a thread of this
+    process, read-only queries), or, where NVML cannot be loaded, from
+    nvidia-smi every 50 ms. Both write the same CSV rows."""
 
     FIELDS = ("timestamp,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
               "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+    NVML_PERIOD_S = 0.001
 
     def __init__(self, index, out_path=None):
         self.index = index
@@ -128,17 +178,49 @@ class ClockSampler:
         self.out_path = out_path
         self.proc = None
         self.f = None
+        self.thread = None
+        self.stop = None
+        self.source = "unsampled"
         self.regions = []
 
+    def _nvml_loop(self, nv):
+        import datetime
+        order = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
+        while not self.stop.is_set():
+            t = time.time()
+            r = nv.sample()
+            if r is not None:
+                clk, watts, mask = r
+                seen = {name for bit, name in nv.REASONS.items() if mask & bit}
+                stamp = datetime.datetime.fromtimestamp(t).strftime("%Y/%m/%d %H:%M:%S.%f")
+                self.f.write("%s, %d, %d, %.2f, 0x%x, %s\n" % (
+                    stamp, clk, nv.max_mhz, watts, mask,
+                    ", ".join("Active" if n in seen else "Not Active" for n in order)))
+            time.sleep(self.NVML_PERIOD_S)
+        nv.close()
+
     def __enter__(self):
+        import threading
         try:
             self.f = open(self.out_path, "w")
-            self.proc = subprocess.Popen(
-                ["nvidia-smi", "-i", str(self.index), "--query-gpu=" + self.FIELDS,
-                 "--format=csv,noheader,nounits", "-lms", "50"],
-                stdout=self.f, stderr=subprocess.DEVNULL)
         except OSError:
-            self.proc = None
+            self.f = None
+            return self
+        nv = _NvmlClocks(self.index)
+        if nv.ok:
+            self.stop = threading.Event()
+            self.thread = threading.Thread(target=self._nvml_loop, args=(nv,), daemon=True)
+            self.thread.start()
+            self.source = "NVML, every 1 ms"
+        else:
+            try:
+                self.proc = subprocess.Popen(
+                    ["nvidia-smi", "-i", str(self.index), "--query-gpu=" + self.FIELDS,
+                     "--format=csv,noheader,nounits", "-lms", "50"],
+                    stdout=self.f, stderr=subprocess.DEVNULL)
+                self.source = "nvidia-smi, every 50 ms"
+            except OSError:
+                self.proc = None
         time.sleep(0.3)
         return self
 
@@ -147,6 +229,9 @@ class ClockSampler:
         self.regions.append((t0, t1))
 
     def __exit__(self, *a):
+        if self.thread is not None:
+            self.stop.set()
+            self.thread.join(timeout=5)
         if self.proc is not None:
             time.sleep(0.1)
             self.proc.terminate()
@@ -159,6 +244,7 @@ class ClockSampler:
 
     def summary(self, region=None):
         out = summarize_clocks(self.out_path, [region] if region else self.regions)
+        out["source"] = self.source
         return out
 
     def cleanup(self):
@@ -183,9 +269,9 @@ def _stamp(text):
 def summarize_clocks(path, regions):
     """Median SM clock, the maximum and every throttle reason seen, over the
     samples whose timestamp falls inside one of the timed regions. With no
-    sample inside (a region shorter than the 50 ms sampling interval), the
-    clock is reported as None and the nearest samples (within 0.25 s of a
-    region) are summarised separately, labelled as such."""
+    sample inside (a region shorter than the sampling interval), the clock
+    is reported as None and the nearest samples (within 0.25 s of a region)
+    are summarised separately, labelled as such."""
     names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
     rows = []
     try:
@@ -220,7 +306,7 @@ def summarize_clocks(path, regions):
     near = pick(0.25)
     out = {"sm_mhz": None, "sm_max_mhz": max(r[2] for r in rows), "reasons": [], "samples": 0,
            "timed_region_s": timed_s,
-           "note": "no nvidia-smi sample (50 ms interval) fell inside the timed region"}
+           "note": "no clock sample fell inside the timed region"}
     if near:
         out["within_0.25s_of_timed_region"] = summ(near)
     return out

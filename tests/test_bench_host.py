@@ -36,7 +36,7 @@ def test_clock_summary_says_so_when_no_sample_is_inside(tmp_path):
     p.write_text(_clock_lines())
     t = bench._stamp("2026/12/02 10:00:00.000")
     s = bench.summarize_clocks(str(p), [(t + 0.06, t + 0.08)])   # 20 ms, between two samples
-    assert s["samples"] == 0 and s["sm_mhz"] is None and "no nvidia-smi sample" in s["note"]
+    assert s["samples"] == 0 and s["sm_mhz"] is None and "no clock sample" in s["note"]
     assert s["within_0.25s_of_timed_region"]["samples"] == 4
 
 
@@ -106,3 +106,40 @@ def test_cpu_baseline_reports_all_cores_and_one_core():
     assert st["cores"] == 1 and st["value"] > 0
     import oracle
     assert oracle.num_threads() == cb["cores"]  # restored afterwards
+
+
+def test_nvml_sampler_rows_parse_like_nvidia_smi_rows(tmp_path):
+    """The 1 ms sampler's rows (written from a stand-in for the NVML queries)
+    go through the same summary: clock, maximum and the reasons' bits."""
+    import threading
+    import time
+
+    class FakeNvml:
+        REASONS = bench._NvmlClocks.REASONS
+        max_mhz = 2070
+
+        def __init__(self):
+            self.closed = False
+
+        def sample(self):
+            return 1980, 912.5, 0x4 | 0x1   # power cap, and an idle bit that is not reported
+
+        def close(self):
+            self.closed = True
+
+    cs = bench.ClockSampler(0, str(tmp_path / "c.csv"))
+    cs.f = open(cs.out_path, "w")
+    cs.stop = threading.Event()
+    nv = FakeNvml()
+    th = threading.Thread(target=cs._nvml_loop, args=(nv,))
+    t0 = time.time()
+    th.start()
+    time.sleep(0.05)
+    t1 = time.time()
+    cs.stop.set()
+    th.join()
+    cs.f.close()
+    s = bench.summarize_clocks(cs.out_path, [(t0, t1)])
+    assert s["samples"] >= 5
+    assert s["sm_mhz"] == 1980 and s["sm_max_mhz"] == 2070 and s["reasons"] == ["sw_power_cap"]
+    assert nv.closed
