@@ -732,6 +732,14 @@ def run_ours(args):
     if "frac_hbm" in dk:
         roofline.update(achieved_gbs=dk["achieved_gbs"], frac_hbm=dk["frac_hbm"], hbm_peak=hbm)
     quant = next((k for k in kernels if k["part"].startswith("quant_x")), None)
+    if quant is not None and n == 2:
+        # quantise + one GEMM: what the quantiser adds to the step beyond the
+        # GEMM's own time (the GEMM is launched under the quantiser's tail)
+        gemm_ms = part_ms[1 - parts.index(next(p_ for p_ in parts if p_.name.startswith("quant_x")))]
+        quant = dict(quant, step_minus_gemm_us=round((ms_step - gemm_ms) * 1e3, 1),
+                     step_minus_gemm_note="whole-step time minus the GEMM's own event time: the quantiser "
+                                          "and the launch gap; the GEMM sets itself up under the quantiser's "
+                                          "last wave (programmatic dependent launch)")
     line = {
         "metric": METRIC,
         "value": round(value, 2),
