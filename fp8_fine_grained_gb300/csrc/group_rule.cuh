@@ -60,10 +60,4 @@ __device__ __forceinline__ ScalePair group_scale_rule(float amax)
         return group_scale(amax);
 }
 
-// two bf16 values (the low and high half of w) -> two E4M3 bytes
-__device__ __forceinline__ uint32_t quant2(uint32_t w, float inv)
-{
-    return cvt_e4m3x2(__fmul_rn(bf16_lo(w), inv), __fmul_rn(bf16_hi(w), inv));
-}
-
 }  // namespace fp8fg
