@@ -10,6 +10,7 @@ If the library is missing or fails to load, every call raises.
 Entry points (same names as the C ABI):
     fp8_quant_1x128(x, transpose=False)     -> (q, scales)
     fp8_quant_128x128(w)                    -> (q, scales)
+    fp8_quant_128x128_dual(w)               -> (q, scales, qT, scalesT)
     fp8_gemm_blockscaled(mode, a, sa, b, sb, out_dtype) -> C
     fp8_grouped_gemm(xq, sx, row_index, expert_offsets, wq, sw, n_rows, out_dtype) -> Y
 plus the convenience wrappers fprop / dgrad / wgrad and device_status().
@@ -45,6 +46,8 @@ def lib():
         L.fp8_quant_1x128_gather.argtypes = [P, I64, I64, I64, P, I64, P, I64, P, I64, P]
         L.fp8_quant_1x128_dual.argtypes = [P, I64, I64, I64, P, I64, P, I64, P, I64, P, I64, P]
         L.fp8_quant_128x128.argtypes = [P, I64, I64, I64, P, I64, P, P]
+        L.fp8_quant_128x128_dual.argtypes = [P, I64, I64, I64, P, I64, P, P, I64, P, P]
+        L.fp8_quant_128x128_dual_pow2.argtypes = [P, I64, I64, I64, P, I64, P, P, I64, P, P]
         L.fp8_quant_1x128_pow2.argtypes = L.fp8_quant_1x128.argtypes
         L.fp8_quant_1x128_gather_pow2.argtypes = L.fp8_quant_1x128_gather.argtypes
         L.fp8_quant_1x128_dual_pow2.argtypes = L.fp8_quant_1x128_dual.argtypes
@@ -363,6 +366,39 @@ def fp8_quant_128x128(w, q=None, scales=None, stream=None, pow2=False):
     rc = fn(_ptr(w2), N, K, w2.stride(0), _ptr(q2), q2.stride(0), _ptr(scales), _stream(stream))
     _check(rc, "fp8_quant_128x128_pow2" if pow2 else "fp8_quant_128x128")
     return q, scales
+
+
+def fp8_quant_128x128_dual(w, q=None, scales=None, qT=None, scalesT=None, stream=None, pow2=False):
+    """128x128 blocks of a bf16 weight [N, K] and of its transpose from one
+    read: returns (q [N, K], scales [N/128, K/128], qT [K, N], scalesT
+    [K/128, N/128]), equal to fp8_quant_128x128(w) and
+    fp8_quant_128x128(w.t()) (with the same pow2 choice)."""
+    torch = _torch()
+    _layout(w, "w")
+    if w.dim() != 2 or w.dtype != torch.bfloat16:
+        raise ValueError("w must be a 2-D bfloat16 tensor")
+    N, K = w.shape
+    dev = w.device
+    q = torch.empty((N, K), dtype=torch.uint8, device=dev) if q is None else q
+    scales = torch.empty((N // 128, K // 128), dtype=torch.float32, device=dev) if scales is None else scales
+    qT = torch.empty((K, N), dtype=torch.uint8, device=dev) if qT is None else qT
+    scalesT = torch.empty((K // 128, N // 128), dtype=torch.float32, device=dev) if scalesT is None else scalesT
+    for t, name, dt in ((q, "q", torch.uint8), (qT, "qT", torch.uint8), (scales, "scales", torch.float32),
+                        (scalesT, "scalesT", torch.float32)):
+        _dtype(t, dt, name)
+    _layout(q, "q")
+    _layout(qT, "qT")
+    _at_least(q, N, K, "q")
+    _at_least(qT, K, N, "qT")
+    if not scales.is_contiguous() or not scalesT.is_contiguous() or scales.numel() < (N // 128) * (K // 128) \
+            or scalesT.numel() < (N // 128) * (K // 128):
+        raise ValueError("scales and scalesT must be contiguous and hold [N/128, K/128] float32")
+    _on_gpu((w, "w"), (q, "q"), (scales, "scales"), (qT, "qT"), (scalesT, "scalesT"))
+    fn = lib().fp8_quant_128x128_dual_pow2 if pow2 else lib().fp8_quant_128x128_dual
+    rc = fn(_ptr(w), N, K, w.stride(0), _ptr(q), q.stride(0), _ptr(scales), _ptr(qT), qT.stride(0), _ptr(scalesT),
+            _stream(stream))
+    _check(rc, "fp8_quant_128x128_dual_pow2" if pow2 else "fp8_quant_128x128_dual")
+    return q, scales, qT, scalesT
 
 
 # ----------------------------------------------------------------- GEMM ----

@@ -517,13 +517,21 @@ __global__ void __launch_bounds__(256, DUAL_CTAS_PER_SM)
 
 // ------------------------------------------------------- 128x128 blocks ----
 // One CTA per block: 256 threads x 8 chunks of 8 bf16 held in registers.
-template <bool P2>
-__global__ void __launch_bounds__(256) quant_blocks_kernel(const uint16_t *__restrict__ w, int64_t K, int64_t ldw,
-                                                           uint8_t *__restrict__ q, int64_t ldq,
-                                                           float *__restrict__ scales)
+// DUAL: the transposed codes too (the block of W^T is the transposed block
+// with the same scale): the codes go through a shared-memory tile and each
+// thread writes 64 codes of one column of the block as a piece of the
+// transposed row.
+constexpr int QB_PITCH = GROUP + 8;  // bytes per row of the code tile (8-byte aligned rows)
+
+template <bool P2, bool DUAL>
+__global__ void __launch_bounds__(256) quant_blocks_kernel(const uint16_t *__restrict__ w, int64_t N, int64_t K,
+                                                           int64_t ldw, uint8_t *__restrict__ q, int64_t ldq,
+                                                           float *__restrict__ scales, uint8_t *__restrict__ qT,
+                                                           int64_t ldqT, float *__restrict__ scalesT)
 {
     griddep_launch_dependents();  // a dependent GEMM may set itself up under this grid's tail
     __shared__ uint32_t s_warp[8];
+    __shared__ __align__(16) uint8_t s_codes[DUAL ? GROUP * QB_PITCH : 8];
     const int tid = threadIdx.x;
     const int64_t bj = blockIdx.x, bi = blockIdx.y;
     const uint16_t *src = w + bi * GROUP * ldw + bj * GROUP;
@@ -553,10 +561,33 @@ __global__ void __launch_bounds__(256) quant_blocks_kernel(const uint16_t *__res
 #pragma unroll
     for (int i = 0; i < 8; ++i) {
         const int chunk = i * 256 + tid;
-        *reinterpret_cast<uint2 *>(dst + (chunk >> 4) * ldq + (chunk & 15) * 8) = quant8(v[i], sp.inv);
+        const uint2 c8 = quant8(v[i], sp.inv);
+        *reinterpret_cast<uint2 *>(dst + (chunk >> 4) * ldq + (chunk & 15) * 8) = c8;
+        if constexpr (DUAL)
+            *reinterpret_cast<uint2 *>(s_codes + (chunk >> 4) * QB_PITCH + (chunk & 15) * 8) = c8;
     }
-    if (tid == 0)
+    if (tid == 0) {
         scales[bi * (K / GROUP) + bj] = sp.s;
+        if constexpr (DUAL)
+            scalesT[bj * (N / GROUP) + bi] = sp.s;
+    }
+    if constexpr (DUAL) {
+        __syncthreads();
+        // thread: column c of the block (a warp reads 32 consecutive bytes
+        // of a row), rows h*64 .. +63 -> qT row (block column c), 64 codes
+        const int c = tid & (GROUP - 1), h = tid >> 7;
+        uint32_t wv[16];
+#pragma unroll
+        for (int j = 0; j < 16; ++j) {
+            const uint8_t *col = s_codes + (h * 64 + 4 * j) * QB_PITCH + c;
+            wv[j] = (uint32_t)col[0] | ((uint32_t)col[QB_PITCH] << 8) | ((uint32_t)col[2 * QB_PITCH] << 16) |
+                    ((uint32_t)col[3 * QB_PITCH] << 24);
+        }
+        uint4 *out = reinterpret_cast<uint4 *>(qT + (bj * GROUP + c) * ldqT + bi * GROUP + h * 64);
+#pragma unroll
+        for (int j = 0; j < 4; ++j)
+            out[j] = make_uint4(wv[4 * j], wv[4 * j + 1], wv[4 * j + 2], wv[4 * j + 3]);
+    }
 }
 
 // ----------------------------------------------------------- entry points ----
@@ -719,8 +750,31 @@ int quant_128x128(const void *w, int64_t N, int64_t K, int64_t ldw, uint8_t *q, 
     const int64_t gx = K / GROUP, gy = N / GROUP;
     if (gx > 0x7FFFFFFF || gy > 65535)
         return FP8FG_EINVAL;
-    quant_blocks_kernel<P2><<<dim3((unsigned)gx, (unsigned)gy), 256, 0, static_cast<cudaStream_t>(stream)>>>(
-        static_cast<const uint16_t *>(w), K, ldw, q, ldq, scales);
+    quant_blocks_kernel<P2, false><<<dim3((unsigned)gx, (unsigned)gy), 256, 0, static_cast<cudaStream_t>(stream)>>>(
+        static_cast<const uint16_t *>(w), N, K, ldw, q, ldq, scales, nullptr, 0, nullptr);
+    return launch_status();
+}
+
+template <bool P2>
+int quant_128x128_dual(const void *w, int64_t N, int64_t K, int64_t ldw, uint8_t *q, int64_t ldq, float *scales,
+                       uint8_t *qT, int64_t ldqT, float *scalesT, void *stream)
+{
+    if (N < 0 || K < 0 || N % GROUP != 0 || K % GROUP != 0 || ldw < K || ldq < K || ldqT < N)
+        return FP8FG_EINVAL;
+    if (N == 0 || K == 0)
+        return FP8FG_OK;
+    if (!w || !q || !scales || !qT || !scalesT)
+        return FP8FG_EINVAL;
+    if (!aligned16(w) || !aligned16(q) || !aligned16(qT) || ldw % 8 != 0 || ldq % 16 != 0 || ldqT % 16 != 0 ||
+        (reinterpret_cast<uintptr_t>(scales) & 3u) != 0 || (reinterpret_cast<uintptr_t>(scalesT) & 3u) != 0)
+        return FP8FG_EALIGN;
+    if (!device_supported())
+        return FP8FG_EUNSUPPORTED;
+    const int64_t gx = K / GROUP, gy = N / GROUP;
+    if (gx > 0x7FFFFFFF || gy > 65535)
+        return FP8FG_EINVAL;
+    quant_blocks_kernel<P2, true><<<dim3((unsigned)gx, (unsigned)gy), 256, 0, static_cast<cudaStream_t>(stream)>>>(
+        static_cast<const uint16_t *>(w), N, K, ldw, q, ldq, scales, qT, ldqT, scalesT);
     return launch_status();
 }
 
@@ -793,4 +847,17 @@ extern "C" int fp8_quant_128x128_pow2(const void *w, int64_t N, int64_t K, int64
                                       float *scales, void *stream)
 {
     return quant_128x128<true>(w, N, K, ldw, q, ldq, scales, stream);
+}
+
+extern "C" int fp8_quant_128x128_dual(const void *w, int64_t N, int64_t K, int64_t ldw, uint8_t *q, int64_t ldq,
+                                      float *scales, uint8_t *qT, int64_t ldqT, float *scalesT, void *stream)
+{
+    return quant_128x128_dual<false>(w, N, K, ldw, q, ldq, scales, qT, ldqT, scalesT, stream);
+}
+
+extern "C" int fp8_quant_128x128_dual_pow2(const void *w, int64_t N, int64_t K, int64_t ldw, uint8_t *q,
+                                           int64_t ldq, float *scales, uint8_t *qT, int64_t ldqT, float *scalesT,
+                                           void *stream)
+{
+    return quant_128x128_dual<true>(w, N, K, ldw, q, ldq, scales, qT, ldqT, scalesT, stream);
 }

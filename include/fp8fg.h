@@ -202,6 +202,30 @@ FP8FG_API int fp8_quant_128x128(const void *w, int64_t N, int64_t K, int64_t ldw
                       uint8_t *q, int64_t ldq, float *scales, void *stream);
 
 /* ---------------------------------------------------------------------
+ * fp8_quant_128x128_dual: the weight's 128x128 blocks and those of its
+ * transpose from one read of w.
+ * Source: innerforce.co.kr, fine-grained quantization paragraph (128x128
+ * weight blocks); tonho.wtf "o que isso custou" (a fused cast and a
+ * transposed read on the wish list). The block (j, i) of W^T is the
+ * transpose of block (i, j) of W with the same scale, so qT and scalesT
+ * equal fp8_quant_128x128 of the materialised transpose, byte for byte.
+ *
+ *   w, q, scales  as fp8_quant_128x128 (W [N][K]).
+ *   qT       E4M3 bytes [K][ldqT], ldqT >= N: qT[k][n] = q[n][k].
+ *   scalesT  FP32 [K/128][N/128], dense: scalesT[j*(N/128) + i] =
+ *            scales[i*(K/128) + j].
+ *   Alignment: w, q, qT 16-byte aligned; ldw % 8 == 0, ldq % 16 == 0,
+ *   ldqT % 16 == 0; scales and scalesT 4-byte aligned.
+ *   Errors: FP8FG_EINVAL for N or K not a multiple of 128 or a leading
+ *   dimension below its minimum; FP8FG_EALIGN as above. All buffers are
+ *   owned by the caller. fp8_quant_128x128_dual_pow2 is the power-of-two
+ *   variant (see below).
+ * ------------------------------------------------------------------- */
+FP8FG_API int fp8_quant_128x128_dual(const void *w, int64_t N, int64_t K, int64_t ldw,
+                      uint8_t *q, int64_t ldq, float *scales,
+                      uint8_t *qT, int64_t ldqT, float *scalesT, void *stream);
+
+/* ---------------------------------------------------------------------
  * fp8_gemm_blockscaled: block-scaled FP8 GEMM, promotion every 128 of the
  * contraction dimension K.
  * Source: innerforce.co.kr, increased-precision accumulation paragraph
@@ -319,9 +343,10 @@ FP8FG_API int fp8_grouped_gemm(const uint8_t *Xq, const float *sX, int64_t ld_sX
  *
  * fp8_quant_1x128_pow2, fp8_quant_1x128_dual_pow2,
  * fp8_quant_1x128_gather_pow2, fp8_quant_1x128_scatter_pow2,
- * fp8_quant_128x128_pow2: arguments, layouts, alignment and errors exactly
- * as fp8_quant_1x128, fp8_quant_1x128_dual, fp8_quant_1x128_gather,
- * fp8_quant_1x128_scatter and fp8_quant_128x128; only the scale rule
+ * fp8_quant_128x128_pow2, fp8_quant_128x128_dual_pow2: arguments,
+ * layouts, alignment and errors exactly as fp8_quant_1x128,
+ * fp8_quant_1x128_dual, fp8_quant_1x128_gather, fp8_quant_1x128_scatter,
+ * fp8_quant_128x128 and fp8_quant_128x128_dual; only the scale rule
  * differs.
  * ------------------------------------------------------------------- */
 FP8FG_API int fp8_quant_1x128_pow2(const void *x, int64_t rows, int64_t cols, int64_t ldx,
@@ -339,6 +364,9 @@ FP8FG_API int fp8_quant_1x128_scatter_pow2(const void *x, int64_t n_src, int64_t
                          uint8_t *q, int64_t ldq, float *scales, int64_t ld_s, void *stream);
 FP8FG_API int fp8_quant_128x128_pow2(const void *w, int64_t N, int64_t K, int64_t ldw,
                          uint8_t *q, int64_t ldq, float *scales, void *stream);
+FP8FG_API int fp8_quant_128x128_dual_pow2(const void *w, int64_t N, int64_t K, int64_t ldw,
+                      uint8_t *q, int64_t ldq, float *scales,
+                      uint8_t *qT, int64_t ldqT, float *scalesT, void *stream);
 
 /* ---------------------------------------------------------------------
  * fp8_gemm_mx: the GEMM of fp8_gemm_blockscaled (same modes, operands,

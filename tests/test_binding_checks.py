@@ -131,6 +131,11 @@ def test_quantiser_outputs_checked():
     expect("scalesT must cover", fg.fp8_quant_1x128_dual, x, scalesT=z((2, 380), F32))
     w = z((256, 384), BF16)
     expect("q must be", fg.fp8_quant_128x128, w, q=z((128, 384), U8))
+    expect("qT must cover", fg.fp8_quant_128x128_dual, w, qT=z((384, 128), U8))
+    expect("q must cover", fg.fp8_quant_128x128_dual, w, q=z((256, 256), U8))
+    expect("scales and scalesT", fg.fp8_quant_128x128_dual, w, scalesT=z((3, 1), F32))
+    expect("qT must be", fg.fp8_quant_128x128_dual, w, qT=z((384, 256), I32))
+    expect("w must be a 2-D", fg.fp8_quant_128x128_dual, z((2, 256, 384), BF16))
 
 
 def test_grouped_tile_count_limit_in_the_abi():

@@ -80,6 +80,19 @@ def test_quant_128x128_validation(L):
     assert f(A16, 0, 128, 128, A16, 128, A16, NULL) == 0
 
 
+@pytest.mark.parametrize("entry", ["fp8_quant_128x128_dual", "fp8_quant_128x128_dual_pow2"])
+def test_quant_128x128_dual_validation(L, entry):
+    f = getattr(L, entry)
+    # w, N, K, ldw, q, ldq, scales, qT, ldqT, scalesT
+    assert f(A16, 100, 128, 128, A16, 128, A16, A16, 128, A16, NULL) == EINVAL    # N % 128
+    assert f(A16, 128, 130, 130, A16, 130, A16, A16, 128, A16, NULL) == EINVAL    # K % 128
+    assert f(A16, 256, 128, 128, A16, 128, A16, A16, 128, A16, NULL) == EINVAL    # ldqT < N
+    assert f(A16, 128, 128, 128, A16, 128, A16, A8, 128, A16, NULL) == EALIGN     # qT
+    assert f(A16, 128, 128, 128, A16, 128, A16, A16, 136, A16, NULL) == EALIGN    # ldqT % 16
+    assert f(A16, 128, 128, 128, A16, 128, A16, NULL, 128, A16, NULL) == EINVAL   # missing qT
+    assert f(A16, 0, 128, 128, A16, 128, A16, A16, 128, A16, NULL) == 0
+
+
 def gemm(L, **kw):
     a = dict(mode=0, A=A16, sA=A16, lda=256, ldsa=128, B=A16, sB=A16, ldb=256, ldsb=2, M=128, N=256, K=256,
              C=A16, out=1, ldc=256)

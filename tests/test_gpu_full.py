@@ -26,6 +26,19 @@ def _sample(n, k, seed):
     return np.unique(np.concatenate([rng.choice(n, k, replace=False), [0, n - 1]]))
 
 
+def test_trio_weight_dual_full_size():
+    """The trio's weight (18432 x 7168) and its transpose from one read,
+    both bit-exact: the transposed blocks against the oracle's quantisation
+    of the materialised W^T."""
+    _, w, _ = synth.trio(seed=0, device=DEV)
+    q, s, qT, sT = fg.fp8_quant_128x128_dual(w)
+    torch.cuda.synchronize()
+    qo, so = oracle.quant_128x128(bits(w))
+    assert np.array_equal(to_np(q), qo) and np.array_equal(to_np(s).view(np.uint32), so.view(np.uint32))
+    qTo, sTo = oracle.quant_128x128(bits(w.t().contiguous()))
+    assert np.array_equal(to_np(qT), qTo) and np.array_equal(to_np(sT).view(np.uint32), sTo.view(np.uint32))
+
+
 def test_trio_full_size():
     x, w, dy = synth.trio(seed=0, device=DEV)
     M, K = x.shape

@@ -85,6 +85,42 @@ def test_quant_128x128(N, K):
     assert np.array_equal(to_np(s).view(np.uint32), so.view(np.uint32))
 
 
+@pytest.mark.parametrize("N,K", [(128, 128), (256, 384), (384, 256), (1024, 2048)])
+@pytest.mark.parametrize("pow2", [False, True])
+def test_quant_128x128_dual(N, K, pow2):
+    """Both the weight's blocks and those of its transpose from one read:
+    q and scales equal the oracle's quantisation of W, qT and scalesT the
+    oracle's quantisation of the materialised W^T (computed independently,
+    not by transposing q)."""
+    g = torch.Generator(device=DEV)
+    g.manual_seed(N * 3 + K + pow2)
+    w = (torch.randn(N, K, generator=g, device=DEV) * 0.02)
+    w[:128, -128:] *= 40
+    w = w.to(torch.bfloat16)
+    q, s, qT, sT = fg.fp8_quant_128x128_dual(w, pow2=pow2)
+    torch.cuda.synchronize()
+    qo, so = oracle.quant_128x128(bits(w), pow2=pow2)
+    qTo, sTo = oracle.quant_128x128(bits(w.t().contiguous()), pow2=pow2)
+    assert np.array_equal(to_np(q), qo)
+    assert np.array_equal(to_np(s).view(np.uint32), so.view(np.uint32))
+    assert np.array_equal(to_np(qT), qTo)
+    assert np.array_equal(to_np(sT).view(np.uint32), sTo.view(np.uint32))
+
+
+def test_quant_128x128_dual_pitched_outputs():
+    """Output pitches larger than the matrix: the padding stays untouched."""
+    g = torch.Generator(device=DEV)
+    g.manual_seed(9)
+    w = (torch.randn(256, 384, generator=g, device=DEV) * 0.02).to(torch.bfloat16)
+    qbuf = torch.full((256, 400), 7, dtype=torch.uint8, device=DEV)
+    qTbuf = torch.full((384, 272), 7, dtype=torch.uint8, device=DEV)
+    q, s, qT, sT = fg.fp8_quant_128x128_dual(w, q=qbuf[:, :384], qT=qTbuf[:, :256])
+    torch.cuda.synchronize()
+    assert torch.all(qbuf[:, 384:] == 7) and torch.all(qTbuf[:, 256:] == 7)
+    qo, _ = oracle.quant_128x128(bits(w))
+    assert np.array_equal(to_np(qbuf[:, :384]), qo) and np.array_equal(to_np(qTbuf[:, :256]), qo.T)
+
+
 def test_quant_128x128_experts_3d():
     g = torch.Generator(device=DEV)
     g.manual_seed(5)
