@@ -380,7 +380,7 @@ __global__ void __launch_bounds__(256, DUAL_CTAS_PER_SM)
     quant_dual_kernel(const __grid_constant__ CUtensorMap tmx, int64_t tiles_c, int64_t n_tiles,
                       uint8_t *__restrict__ q, int64_t ldq, float *__restrict__ scales, int64_t ld_s,
                       uint8_t *__restrict__ qT, int64_t ldqT, float *__restrict__ scalesT, int64_t ld_sT, int *status,
-                      uint64_t wait_limit_ns)
+                      uint64_t wait_limit_ns, int skip_first_load)
 {
     griddep_launch_dependents();  // a dependent GEMM may set itself up under this grid's tail
     extern __shared__ __align__(128) uint8_t dual_raw[];
@@ -402,7 +402,9 @@ __global__ void __launch_bounds__(256, DUAL_CTAS_PER_SM)
         tma_load_2d(smem_u32(&S.tile[b][0][0]), &tmx, (int32_t)((t % tiles_c) * GROUP),
                     (int32_t)((t / tiles_c) * GROUP), bar0 + 8 * b);
     };
-    if (tid == 0 && (int64_t)blockIdx.x < n_tiles)
+    // (test hook: CTA 0 withholds its first copy, so that its bounded wait
+    // runs out and the launch reports FP8FG_ETIMEOUT)
+    if (tid == 0 && (int64_t)blockIdx.x < n_tiles && !(skip_first_load && blockIdx.x == 0))
         fetch(blockIdx.x, 0);
     uint32_t it = 0;
     for (int64_t t = blockIdx.x; t < n_tiles; t += gridDim.x, ++it) {
@@ -728,7 +730,8 @@ int quant_1x128_dual(const void *x, int64_t rows, int64_t cols, int64_t ldx, uin
     const int64_t cap = (int64_t)sm_count() * DUAL_CTAS_PER_SM;
     const unsigned grid = (unsigned)(n_tiles < cap ? n_tiles : (cap > 0 ? cap : 1));
     k<<<grid, 256, sizeof(DualSmem), static_cast<cudaStream_t>(stream)>>>(
-        tmx, tiles_c, n_tiles, q, ldq, scales, ld_s, qT, ldqT, scalesT, ld_sT, status, wait_limit_ns());
+        tmx, tiles_c, n_tiles, q, ldq, scales, ld_s, qT, ldqT, scalesT, ld_sT, status, wait_limit_ns(),
+        take_skip_first_load() ? 1 : 0);
     return launch_status();
 }
 

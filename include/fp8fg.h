@@ -451,11 +451,11 @@ FP8FG_API int fp8fg_device_status(void *stream);
 /* Library version (major*10000 + minor*100 + patch). */
 FP8FG_API int fp8fg_version(void);
 
-/* Test hook: when `skip` != 0, the next fp8_gemm_blockscaled, fp8_gemm_mx
- * or fp8_grouped_gemm_mx launch on the current device withholds its first
- * operand load (a fp8_grouped_gemm launch clears the request without using
- * it), so the consumers' bounded
- * waits run out and the launch reports FP8FG_ETIMEOUT. One-shot; returns
+/* Test hook: when `skip` != 0, the next fp8_gemm_blockscaled, fp8_gemm_mx,
+ * fp8_grouped_gemm_mx or fp8_quant_1x128_dual(_pow2) launch on the current
+ * device withholds its first operand load (a fp8_grouped_gemm launch
+ * clears the request without using it), so the consumers' bounded waits
+ * run out and the launch reports FP8FG_ETIMEOUT. One-shot; returns
  * FP8FG_OK. For exercising failure detection without a GPU fault. */
 FP8FG_API int fp8fg_test_skip_first_load(int skip);
 

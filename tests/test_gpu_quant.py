@@ -159,6 +159,25 @@ def test_quant_dual(rows, cols):
     assert np.array_equal(to_np(sT)[:, :cols].view(np.uint32), so.view(np.uint32))
 
 
+def test_quant_dual_timeout_is_reported_not_hung():
+    """The dual quantiser's bounded wait on its TMA tile: a withheld copy
+    (test hook) makes it run out, the launch reports FP8FG_ETIMEOUT, and the
+    next launch is clean and bit-exact."""
+    x = _x(1024, 1024, seed=3)
+    fg.set_wait_limit_ns(50_000_000)
+    try:
+        fg.inject_skip_first_load(True)
+        fg.fp8_quant_1x128_dual(x)
+        assert fg.device_status() == 5  # FP8FG_ETIMEOUT
+        q, s, qT, sT = fg.fp8_quant_1x128_dual(x)
+        assert fg.device_status() == 0
+    finally:
+        fg.set_wait_limit_ns(2_000_000_000)
+    assert_quant_1x128(x, q, s)
+    qo, so = oracle.quant_128x1_t(bits(x))
+    assert np.array_equal(to_np(qT), qo) and np.array_equal(to_np(sT)[:, :1024].view(np.uint32), so.view(np.uint32))
+
+
 def test_quant_dual_pitched_outputs():
     base = _x(256, 640, seed=9)
     x = base[:, :512]
