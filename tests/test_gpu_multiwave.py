@@ -261,3 +261,16 @@ def test_trio_full_size_dual_quantiser():
     wrows = np.unique(np.concatenate([rng.choice(N, 6, replace=False), [0, 255, 256, N - 1]]))
     c, _, t = oracle.wgrad(dyoT, sdyoT, xoT, sxoT, rows=wrows)
     check_gemm(to_np(dw[torch.from_numpy(wrows).to(DEV)]), c, t, False, "trio wgrad (dual-quantised)")
+
+
+@pytest.mark.parametrize("form", ["row_index", "expert_order"])
+def test_grouped_half_width_last_tile(form):
+    """N = 384: every expert's last n-tile holds 128 columns of 256."""
+    E, T, K, N = 6, 700, 256, 384
+    g = _gen(43)
+    x = torch.randn(T, K, generator=g, device=DEV).to(torch.bfloat16)
+    w = (torch.randn(E, N, K, generator=g, device=DEV) * 0.02).to(torch.bfloat16)
+    rng = np.random.default_rng(43)
+    counts = np.array([0, 1, 127, 128, 129, 300])
+    row_index, off = _routing(rng, T, counts)
+    _grouped_against_oracle(x, w, row_index, off, form, "grouped, N = 384 (%s)" % form)
