@@ -12,8 +12,8 @@ compare every output element with the oracle:
   three contraction blocks;
 - the grouped MoE GEMM (row-index and expert-order forms) with more than
   400 tiles over experts of 0..400 rows; with 100 experts all inside one
-  128-row tile (500 tiles); and with 2100 experts, 40 of them routed (some
-  past expert 2047);
+  128-row tile (500 tiles); and with 2100 and 4096 experts, 40 of them
+  routed (some past expert 2047);
 - the whole dense projection workload (4096 x 7168 x 7168, bf16 out), all
   rows;
 - the full-size training trio quantised by the dual-output quantiser, as
@@ -196,9 +196,11 @@ def test_grouped_multiwave_single_class(form):
 
 
 @pytest.mark.parametrize("form", ["row_index", "expert_order"])
-def test_grouped_many_experts_plain_order(form):
-    """2100 experts, 40 of them routed, some past expert 2047."""
-    E, T, K, N = 2100, 1000, 384, 256
+@pytest.mark.parametrize("E", [2100, 4096])
+def test_grouped_many_experts_plain_order(form, E):
+    """2100 or 4096 experts (the most the ABI takes), 40 of them routed,
+    some past expert 2047."""
+    T, K, N = 1000, 384, 256
     g = _gen(42)
     x = torch.randn(T, K, generator=g, device=DEV).to(torch.bfloat16)
     w = (torch.randn(E, N, K, generator=g, device=DEV) * 0.02).to(torch.bfloat16)
@@ -208,7 +210,7 @@ def test_grouped_many_experts_plain_order(form):
     counts[used] = rng.integers(1, 400, used.size)
     counts[E - 1] = 129
     row_index, off = _routing(rng, T, counts)
-    _grouped_against_oracle(x, w, row_index, off, form, "grouped, 2100 experts (%s)" % form)
+    _grouped_against_oracle(x, w, row_index, off, form, "grouped, %d experts (%s)" % (E, form))
 
 
 def test_dense_config_every_element():
