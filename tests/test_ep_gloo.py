@@ -1,6 +1,7 @@
 """Expert-parallel FP8 dispatch and combine across two ranks (gloo, CPU).
 
-Each rank holds its own tokens and half of the experts. The test runs the
+Each rank holds its own tokens and an equal share of the experts (two and
+four ranks). The test runs the
 protocol of fp8_fine_grained_gb300.ep (dispatch plan, the count and row
 all-to-alls, the receive layout, the return exchange) with the CPU oracle in
 place of the GPU kernels (1x128 quantisation, the expert GEMM, the combine),
@@ -113,12 +114,12 @@ def _rank(rank, world, port, out, skewed=False):
         dist.destroy_process_group()
 
 
-def _run_two(port, skewed):
+def _run_two(port, skewed, world=2):
     oracle.build.build()
     ctx = mp.get_context("spawn")
     mgr = ctx.Manager()
     out = mgr.dict()
-    procs = [ctx.Process(target=_rank, args=(r, 2, port, out, skewed)) for r in range(2)]
+    procs = [ctx.Process(target=_rank, args=(r, world, port, out, skewed)) for r in range(world)]
     for p in procs:
         p.start()
     for p in procs:
@@ -130,6 +131,18 @@ def _run_two(port, skewed):
 @pytest.fixture(scope="module")
 def two_ranks():
     return _run_two(29500 + (os.getpid() % 1000), False)
+
+
+def test_four_ranks():
+    """Four ranks of two experts each: every token's output equals the
+    single-process layer, and each rank receives exactly what the others
+    route to its experts."""
+    res = _run_two(31700 + (os.getpid() % 1000), False, world=4)
+    for r in range(4):
+        assert res[r]["combine_equal"], "rank %d" % r
+        for src in range(4):
+            assert np.array_equal(res[r]["recv_counts"][src], res[src]["send_counts"][r])
+        assert res[r]["n_recv"] == sum(int(res[src]["send_counts"][r].sum()) for src in range(4))
 
 
 def test_empty_splits_and_a_token_routed_nowhere():
