@@ -1,10 +1,10 @@
-"""Expert-parallel FP8 dispatch and combine across two ranks (gloo, CPU).
+"""Expert-parallel FP8 dispatch and combine across two and four ranks
+(gloo, CPU).
 
-Each rank holds its own tokens and an equal share of the experts (two and
-four ranks). The test runs the
-protocol of fp8_fine_grained_gb300.ep (dispatch plan, the count and row
-all-to-alls, the receive layout, the return exchange) with the CPU oracle in
-place of the GPU kernels (1x128 quantisation, the expert GEMM, the combine),
+Each rank holds its own tokens and an equal share of the experts. The test
+runs the protocol of fp8_fine_grained_gb300.ep (dispatch plan, the count
+and row all-to-alls, the receive layout, the return exchange) with the CPU
+oracle in place of the GPU kernels (1x128 quantisation, the expert GEMM, the combine),
 and checks every token's combined output bit for bit against the same
 layer computed in one process without expert parallelism: every expert row
 is computed from the same codes and scales and combined in the same slot
