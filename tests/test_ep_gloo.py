@@ -205,3 +205,40 @@ def test_receive_layout_lists_rows_expert_by_expert():
     assert lay.row_index.tolist() == [0, 1, 3, 2, 4, 5]
     assert lay.expert_offsets.tolist() == [0, 3, 6]
     assert lay.n_recv == 6
+
+
+@pytest.mark.parametrize("seed", range(6))
+def test_plan_matches_a_brute_force_sort(seed):
+    """dest lists every used (token, slot) exactly once, rows ordered by
+    expert, then token, then slot; the counts per rank and local expert add
+    up (random routings with unused slots, several world sizes)."""
+    rng = np.random.default_rng(seed)
+    world = [1, 2, 4, 8][seed % 4]
+    E = world * int(rng.integers(1, 5))
+    T, k = int(rng.integers(0, 40)), int(rng.integers(1, 6))
+    ids = rng.integers(-1, E, (T, k)).astype(np.int32)
+    plan = ep.plan_dispatch(torch.from_numpy(ids), E, world)
+    order = sorted((int(ids[t, j]), t, j) for t in range(T) for j in range(k) if ids[t, j] >= 0)
+    want = np.full((T, k), -1, np.int64)
+    for row, (_, t, j) in enumerate(order):
+        want[t, j] = row
+    assert np.array_equal(plan.dest.numpy(), want)
+    assert plan.n_send == len(order)
+    counts = np.bincount([e for e, _, _ in order], minlength=E).reshape(world, E // world)
+    assert np.array_equal(plan.send_counts.numpy(), counts)
+
+
+@pytest.mark.parametrize("seed", range(6))
+def test_receive_layout_matches_a_brute_force_walk(seed):
+    """row_index walks the received rows expert by expert, sources
+    ascending inside an expert, each source's rows in arrival order."""
+    rng = np.random.default_rng(100 + seed)
+    R, Er = int(rng.integers(1, 6)), int(rng.integers(1, 5))
+    counts = rng.integers(0, 5, (R, Er))
+    lay = ep.receive_layout(torch.from_numpy(counts))
+    # arrival order: source by source, each source's rows expert by expert
+    arrival = [(s, e) for s in range(R) for e in range(Er) for _ in range(counts[s, e])]
+    want = [i for e in range(Er) for s in range(R) for i, a in enumerate(arrival) if a == (s, e)]
+    assert lay.row_index.tolist() == want
+    assert lay.n_recv == len(arrival)
+    assert lay.expert_offsets.tolist() == [0] + np.cumsum(counts.sum(0)).tolist()
