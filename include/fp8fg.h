@@ -99,7 +99,10 @@ typedef enum { FP8FG_FPROP = 0, FP8FG_DGRAD = 1, FP8FG_WGRAD = 2 } fp8fg_mode;
  *                  group g at scales[g*ld_s + r] (groups outer, rows
  *                  contiguous: the layout the GEMM reads).
  *   transpose = 1: groups are 128 consecutive ROWS of one column and the
- *           output is transposed. rows % 128 == 0, cols >= 0 arbitrary.
+ *           output is transposed. rows % 128 == 0, cols >= 0 arbitrary;
+ *           rows are read in 16-byte pieces, so with cols % 8 != 0 each
+ *           row of x must be readable up to cols rounded up to a multiple
+ *           of 8 (within ldx; the extra columns do not affect the output).
  *           q      E4M3 bytes [cols][ldq], ldq >= rows: q[c*ldq + r].
  *           scales FP32 [rows/128][ld_s], ld_s >= cols: scale of column c,
  *                  group g at scales[g*ld_s + c].
