@@ -488,10 +488,15 @@ def build(workload, dev, seed, fg, synth):
 # ------------------------------------------------------------------ timing ----
 
 def kernel_source_sha():
+    """Hash of every kernel and host source of the library (file names and
+    contents, in name order)."""
     h = hashlib.sha256()
-    for f in ("gemm.cu", "gemm_mx.cu", "quant.cu", "moe.cu", "ptx.cuh", "group_rule.cuh"):
-        with open(os.path.join(ROOT, "fp8_fine_grained_gb300", "csrc", f), "rb") as fh:
-            h.update(fh.read())
+    csrc = os.path.join(ROOT, "fp8_fine_grained_gb300", "csrc")
+    for f in sorted(os.listdir(csrc)):
+        if f.endswith((".cu", ".cuh", ".h", ".cpp")):
+            h.update(f.encode())
+            with open(os.path.join(csrc, f), "rb") as fh:
+                h.update(fh.read())
     return h.hexdigest()[:16]
 
 

@@ -66,9 +66,10 @@ def lib():
         L.fp8fg_version.argtypes = []
         L.fp8fg_test_skip_first_load.argtypes = [I32]
         L.fp8fg_set_wait_limit_ns.argtypes = [I64]
+        L.fp8fg_set_grouped_schedule.argtypes = [I32, I32]
         for f in ("fp8_quant_1x128", "fp8_quant_128x128", "fp8_gemm_blockscaled", "fp8_grouped_gemm",
                   "fp8fg_device_status", "fp8fg_version", "fp8fg_test_skip_first_load",
-                  "fp8fg_set_wait_limit_ns"):
+                  "fp8fg_set_wait_limit_ns", "fp8fg_set_grouped_schedule"):
             getattr(L, f).restype = I32
         _lib = L
     return _lib
@@ -571,6 +572,15 @@ def device_status(stream=None):
 
 def set_wait_limit_ns(ns):
     _check(lib().fp8fg_set_wait_limit_ns(int(ns)), "fp8fg_set_wait_limit_ns")
+
+
+def set_grouped_schedule(skinny_rows=32, skinny_cost_pct=100):
+    """Schedule of fp8_grouped_gemm with rows in expert order (results do
+    not depend on it): experts with at most `skinny_rows` rows (0: none, at
+    most 32) are computed as 256 weight rows x 32 token rows per tile;
+    `skinny_cost_pct` is such a tile's SM time relative to a full tile, in
+    percent, which sets their share of the SMs. Process-wide."""
+    _check(lib().fp8fg_set_grouped_schedule(int(skinny_rows), int(skinny_cost_pct)), "fp8fg_set_grouped_schedule")
 
 
 def inject_skip_first_load(skip=True):

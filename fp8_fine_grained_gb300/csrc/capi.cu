@@ -21,6 +21,8 @@ struct DeviceCache {
 
 DeviceCache g_dev[kMaxDevices];
 std::atomic<uint64_t> g_wait_limit_ns{2000000000ull};
+std::atomic<int> g_skinny_rows{32};
+std::atomic<int> g_skinny_cost_pct{100};
 std::atomic<int> g_skip_first_load[kMaxDevices];
 
 DeviceCache *cache_for_current()
@@ -70,6 +72,10 @@ bool device_supported()
 }
 
 uint64_t wait_limit_ns() { return g_wait_limit_ns.load(); }
+
+int grouped_skinny_rows() { return g_skinny_rows.load(); }
+
+int grouped_skinny_cost_pct() { return g_skinny_cost_pct.load(); }
 
 bool take_skip_first_load()
 {
@@ -134,6 +140,15 @@ int fp8fg_set_wait_limit_ns(int64_t ns)
     if (ns < 1000000)
         ns = 1000000;
     g_wait_limit_ns.store(static_cast<uint64_t>(ns));
+    return FP8FG_OK;
+}
+
+int fp8fg_set_grouped_schedule(int skinny_rows, int skinny_cost_pct)
+{
+    if (skinny_rows < 0 || skinny_rows > 32 || skinny_cost_pct < 1 || skinny_cost_pct > 1000)
+        return FP8FG_EINVAL;
+    g_skinny_rows.store(skinny_rows);
+    g_skinny_cost_pct.store(skinny_cost_pct);
     return FP8FG_OK;
 }
 

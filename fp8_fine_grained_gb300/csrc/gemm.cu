@@ -117,6 +117,11 @@ struct Params {
     // E4M3 output: scales [N/128][ld_sC]
     float *sC;
     int64_t ld_sC;
+    // experts with rows in expert order: experts with at most skinny_rows
+    // rows take skinny tiles (0: none), and the SM time of a skinny tile
+    // relative to a full one, in percent, divides the CTAs between the two
+    int skinny_rows;
+    int skinny_cost_pct;
 };
 
 // Scale slot of one pipeline stage: the A row scales of the block (a box of
@@ -149,7 +154,8 @@ template <int MODE> struct SmemLayout {
     static constexpr uint32_t tempty_off = tfull_off + 8 * 2;          // one per stage (block g: g % STAGES)
     static constexpr uint32_t tmem_ptr_off = tempty_off + 8 * STAGES;
     static constexpr uint32_t abort_off = tmem_ptr_off + 4;
-    static constexpr uint32_t misc_end = abort_off + 4;
+    static constexpr uint32_t sched_off = (abort_off + 4 + 7) & ~7u;   // the CTA's tile schedule
+    static constexpr uint32_t misc_end = sched_off + 16;
     // per promotion warp: epilogue staging block
     static constexpr uint32_t stage_c_off = (misc_end + 15) & ~15u;
     static constexpr uint32_t stage_c_end = stage_c_off + EPI_WARPS * STAGE_C_BYTES;
@@ -179,6 +185,14 @@ template <int MODE> constexpr uint32_t full_arrivals()
 {
     return MODE == GROUPED ? 1 + GATHER_WARPS : (MODE == WGRAD ? 1 : 2);
 }
+
+// A CTA's tiles: t = first, first + stride, ... below count. The roles read
+// it from shared memory at each tile, so that no register holds it through
+// the contraction loop.
+struct Sched {
+    int64_t count;
+    int first, stride;
+};
 
 struct Tile {
     int64_t m0;       // first A row (dense) / first output row (grouped)
@@ -230,6 +244,300 @@ __device__ __forceinline__ Tile decode_tile(int64_t t, const Params &p, const in
         tl.expert = 0;
     }
     return tl;
+}
+
+// ---------------------------------------------------------------- skinny ----
+// Experts with at most SK_TOK rows (rows in expert order). A full tile of
+// such an expert is 128 token rows of which at most 32 are real. A skinny
+// tile turns the product around: the weight gives the MMA's 128-row side
+// and the tokens its N = 32 side, so one tile is 256 weight rows (two MMAs
+// of M = 128) x 32 tokens, and one pipeline stage carries 32 KB of weights
+// and 4 KB of token codes; five stages fit where the full tiles have four.
+// Both kinds of tile of a small expert stream its weights from DRAM once,
+// and one CTA's stream runs at about 65 GB/s (measured on the MoE layer:
+// about 29 us per skinny tile of 1.8 MB, 31 us per full tile of the same
+// weights); prefetching the boxes into L2 ahead of the ring made both
+// slower. The skinny CTAs run beside the full-tile CTAs, which are bound by
+// their promotion chain instead.
+//
+// The sums are the same: for output (token t, column n), per contraction
+// block kb the tensor cores give P = sum_k W[n,k] X[t,k] and the promotion
+// adds P * (sX[t,kb] * sW[n/128,kb]) into an FP32 sum, with the scale
+// product formed first, as in the full tiles. Roles: warp 0 loads (weights
+// through the B map, tokens through a 32-row map, token scales through the
+// row-scale map, the weight-block scales by cp.async), warp 1 issues, warps
+// 4..11 promote (warp w: TMEM lane quarter w % 4 = 32 weight rows of MMA
+// half (w - 4) / 4, one weight row and the 32 token columns per thread) and
+// store Y[t, n] directly: a warp's 32 consecutive columns of one token row
+// per store.
+constexpr int SK_TOK = 32;                          // token columns of a skinny tile
+constexpr uint32_t SK_X_BYTES = SK_TOK * BK;        // 4 KB of token codes per stage
+
+// CTAs given to the skinny tiles: the grid's share of the estimated SM time
+// (skinny tiles x cost_pct / 100 against full tiles x 1), at least one CTA
+// when there are skinny tiles and one left for the full tiles when there
+// are full tiles; never more CTAs than skinny tiles. Every CTA computes the
+// same value from the same offsets.
+__device__ __forceinline__ int skinny_cta_count(int64_t full_tiles, int64_t skinny_tiles, int grid, int cost_pct)
+{
+    if (skinny_tiles == 0)
+        return 0;
+    int64_t s;
+    if (full_tiles == 0) {
+        s = grid;
+    } else {
+        const int64_t ws = skinny_tiles * cost_pct, wf = full_tiles * 100;
+        s = ((int64_t)grid * ws + (ws + wf) / 2) / (ws + wf);
+        s = s < 1 ? 1 : (s > grid - 1 ? grid - 1 : s);
+    }
+    return (int)(s < skinny_tiles ? s : skinny_tiles);
+}
+
+// Shared memory of a skinny CTA, in the full tiles' allocation: five
+// stages of 32 KB of weights (the four B stages and the first half of the A
+// stages) and 4 KB of token codes (after those, in the A stages), and its
+// barriers and scale slots in the region of the full tiles' epilogue
+// staging blocks, which a skinny CTA does not use. Four TMEM partial
+// buffers of 64 columns (two MMA halves of 32); a buffer's "read" barrier is
+// its block's stage's, which needs no more buffers than stages (see the
+// full tiles' "partial read" barriers).
+struct SkLayout {
+    using L = SmemLayout<GROUPED_C>;
+    static constexpr int STAGES_ = 5;
+    static constexpr int BUFS = 4;
+    static constexpr uint32_t full_off = L::stage_c_off;
+    static constexpr uint32_t empty_off = full_off + 8 * STAGES_;
+    static constexpr uint32_t tfull_off = empty_off + 8 * STAGES_;
+    static constexpr uint32_t tempty_off = tfull_off + 8 * BUFS;
+    static constexpr uint32_t scale_off = (tempty_off + 8 * STAGES_ + 127) & ~127u;
+    static constexpr uint32_t scale_end = scale_off + STAGES_ * ScaleSlot<GROUPED_C>::bytes;
+    static constexpr uint32_t x_off = L::a_off + B_STAGE_BYTES;
+    __device__ static constexpr uint32_t w(int s) { return s < STAGES ? L::b_off + s * B_STAGE_BYTES : L::a_off; }
+    __device__ static constexpr uint32_t x(int s) { return x_off + s * SK_X_BYTES; }
+};
+static_assert(SkLayout::STAGES_ == STAGES + 1, "one weight stage in the A stages");
+static_assert(SkLayout::scale_end <= SmemLayout<GROUPED_C>::stage_c_end, "skinny barriers and scale slots");
+static_assert(SkLayout::x_off + SkLayout::STAGES_ * SK_X_BYTES <= SmemLayout<GROUPED_C>::a_off + STAGES * A_STAGE_BYTES,
+              "skinny token stages");
+static_assert(SkLayout::BUFS <= SkLayout::STAGES_ && SkLayout::BUFS * 2 * SK_TOK <= (int)TMEM_COLS, "skinny buffers");
+
+__device__ __forceinline__ void skinny_init_barriers(uint32_t sbase)
+{
+    for (int s = 0; s < SkLayout::STAGES_; ++s) {
+        mbar_init(sbase + SkLayout::full_off + 8 * s, full_arrivals<GROUPED_C>());
+        mbar_init(sbase + SkLayout::empty_off + 8 * s, EPI_WARPS);
+        mbar_init(sbase + SkLayout::tempty_off + 8 * s, EPI_WARPS);
+    }
+    for (int b = 0; b < SkLayout::BUFS; ++b)
+        mbar_init(sbase + SkLayout::tfull_off + 8 * b, 1);
+    fence_mbar_init();
+}
+
+template <int OUT>
+__device__ __forceinline__ void skinny_roles(const CUtensorMap *tmX, const CUtensorMap *tmW, const CUtensorMap *tmSA,
+                                             const Params &p, uint8_t *smem, const int32_t *prefix,
+                                             volatile const Sched *sched, uint32_t tmem_base, const WaitCtl &wc,
+                                             int warp, int lane)
+{
+    using SK = SkLayout;
+    using SS = ScaleSlot<GROUPED_C>;
+    constexpr int NS = SK::STAGES_, NB = SK::BUFS;
+    const uint32_t sbase = smem_u32(smem);
+    const uint32_t full_bar = sbase + SK::full_off;
+    const uint32_t empty_bar = sbase + SK::empty_off;
+    const uint32_t tfull_bar = sbase + SK::tfull_off;
+    const uint32_t tempty_bar = sbase + SK::tempty_off;
+    const uint32_t scale_base = sbase + SK::scale_off;
+    const int num_kb = (int)(p.K / BK);
+
+    if (warp == 0) {
+        // ------------------------------------------------------ producer ----
+        uint32_t stage = 0, phase = 0;
+        uint32_t filled_mask = 0, fill_parity = 0;
+        bool ok = true;
+        for (int64_t t = sched->first; t < sched->count && ok; t += sched->stride) {
+            const Tile tl = decode_tile<GROUPED_C>(t, p, prefix);
+            for (int kb = 0; kb < num_kb; ++kb) {
+                bool got = true;
+                if (lane == 0)
+                    got = mbar_wait(empty_bar + 8 * stage, phase ^ 1, wc, FP8FG_ETIMEOUT);
+                got = __shfl_sync(0xffffffffu, got ? 1 : 0, 0) != 0;
+                if (!got) {
+                    ok = false;
+                    break;
+                }
+                if (lane == 0) {
+                    const uint32_t fb = full_bar + 8 * stage;
+                    const uint32_t sc_dst = scale_base + stage * SS::bytes;
+                    mbar_arrive_expect_tx(fb, B_STAGE_BYTES + SK_X_BYTES + 4 * SA_BOX);
+                    filled_mask |= 1u << stage;
+                    fill_parity = (fill_parity & ~(1u << stage)) | (phase << stage);
+                    tma_load_2d(sc_dst, tmSA, (int32_t)(tl.m0 & ~int64_t(3)), kb, fb);
+                    cp_async4(sc_dst + SS::b_off, weight_scale<GROUPED_C>(p, tl, kb, 0));
+                    if (tl.n0 + 128 < p.N)
+                        cp_async4(sc_dst + SS::b_off + 4, weight_scale<GROUPED_C>(p, tl, kb, 1));
+                    cp_async_mbar_arrive_noinc(fb);
+                    tma_load_2d(sbase + SK::x(stage), tmX, kb * BK, (int32_t)tl.m0, fb);
+                    tma_load_2d(sbase + SK::w(stage), tmW, kb * BK, (int32_t)(tl.expert * p.N + tl.n0), fb);
+                }
+                __syncwarp();
+                if (++stage == NS) {
+                    stage = 0;
+                    phase ^= 1;
+                }
+            }
+        }
+        asm volatile("cp.async.wait_all;" ::: "memory");
+        if (!ok && lane == 0) {
+            for (int s = 0; s < NS; ++s) {
+                if (!(filled_mask & (1u << s)))
+                    continue;
+                const uint32_t bar = full_bar + 8 * s, par = (fill_parity >> s) & 1u;
+                const uint64_t t0 = global_timer_ns();
+                while (!mbar_try_wait(bar, par) && global_timer_ns() - t0 < wc.limit_ns) {
+                }
+            }
+        }
+    } else if (warp == 1) {
+        // ---------------------------------------------------------- MMA ----
+        constexpr uint32_t IDESC = idesc_e4m3_f32(BM, SK_TOK, false);
+        int committed = 0;
+        uint32_t last_buf = 0, last_par = 0;
+        bool ok = true;
+        int64_t g = 0;
+        uint32_t stage = 0, phase = 0, buf = 0, tphase = 0;
+        for (int64_t t = sched->first; t < sched->count && ok; t += sched->stride) {
+            for (int kb = 0; kb < num_kb; ++kb, ++g) {
+                // buffer `buf` is free once block g - NB has been read out
+                if (g >= NB) {
+                    const int64_t h = g - NB;
+                    const bool got = mbar_wait(tempty_bar + 8 * (uint32_t)(h % NS), (uint32_t)((h / NS) & 1), wc,
+                                               FP8FG_ETIMEOUT);
+                    if (!__all_sync(0xffffffffu, got)) {
+                        ok = false;
+                        break;
+                    }
+                }
+                tc_fence_after();
+                const bool got = mbar_wait(full_bar + 8 * stage, phase, wc, FP8FG_ETIMEOUT);
+                if (!__all_sync(0xffffffffu, got)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                const uint32_t w_addr = sbase + SK::w(stage);
+                const uint32_t x_addr = sbase + SK::x(stage);
+                if (elect_one_sync()) {
+#pragma unroll
+                    for (int h = 0; h < 2; ++h) {
+#pragma unroll
+                        for (int k = 0; k < BK / MMA_K; ++k) {
+                            // both operands K-major with 128-byte rows; the
+                            // weight half h is 128 rows = 16 KB further on
+                            const uint64_t adesc = smem_desc_sw128(w_addr + h * (BM * BK) + k * MMA_K, 0, 1024);
+                            const uint64_t bdesc = smem_desc_sw128(x_addr + k * MMA_K, 0, 1024);
+                            mma_f8f6f4(tmem_base + buf * (2 * SK_TOK) + h * SK_TOK, adesc, bdesc, IDESC,
+                                       k > 0 ? 1u : 0u);
+                        }
+                    }
+                    mma_commit(tfull_bar + 8 * buf);
+                }
+                __syncwarp();
+                committed = 1;
+                last_buf = buf;
+                last_par = tphase;
+                if (++stage == NS) {
+                    stage = 0;
+                    phase ^= 1;
+                }
+                if (++buf == NB) {
+                    buf = 0;
+                    tphase ^= 1;
+                }
+            }
+        }
+        if (!ok && committed && lane == 0) {
+            const uint32_t bar = tfull_bar + 8 * last_buf;
+            const uint64_t t0 = global_timer_ns();
+            while (!mbar_try_wait(bar, last_par) && global_timer_ns() - t0 < wc.limit_ns) {
+            }
+        }
+        __syncwarp();
+    } else if (warp >= EPI_WARP0) {
+        // ------------------------------------------------- promotion ----
+        const int quarter = warp & 3;
+        const int half = (warp - EPI_WARP0) >> 2;
+        uint32_t buf = 0, tphase = 0, stage = 0, phase = 0;
+        bool ok = true;
+        for (int64_t t = sched->first; t < sched->count && ok; t += sched->stride) {
+            const Tile tl = decode_tile<GROUPED_C>(t, p, prefix);
+            const int64_t n = tl.n0 + half * 128 + quarter * 32 + lane;  // this thread's weight row = output column
+            const bool half_ok = tl.n0 + half * 128 < p.N;
+            const int64_t left = tl.row_end - tl.m0;
+            const int nrows = left < SK_TOK ? (int)left : SK_TOK;
+            const uint32_t x0 = 4 * (uint32_t)(tl.m0 & 3);               // first token scale in the slot
+            float2 acc[SK_TOK / 2];
+#pragma unroll
+            for (int j = 0; j < SK_TOK / 2; ++j)
+                acc[j] = make_float2(0.0f, 0.0f);
+            for (int kb = 0; kb < num_kb; ++kb) {
+                bool got = mbar_wait(full_bar + 8 * stage, phase, wc, FP8FG_ETIMEOUT);
+                if (!__all_sync(0xffffffffu, got)) {
+                    ok = false;
+                    break;
+                }
+                const uint8_t *slot = smem + SK::scale_off + stage * SS::bytes;
+                const float sw = reinterpret_cast<const float *>(slot + SS::b_off)[half];
+                const float *sx = reinterpret_cast<const float *>(slot + x0);
+                float2 sc[SK_TOK / 2];
+#pragma unroll
+                for (int j = 0; j < SK_TOK / 2; ++j)
+                    sc[j] = make_float2(__fmul_rn(sx[2 * j], sw), __fmul_rn(sx[2 * j + 1], sw));
+                got = mbar_wait(tfull_bar + 8 * buf, tphase, wc, FP8FG_ETIMEOUT);
+                if (!__all_sync(0xffffffffu, got)) {
+                    ok = false;
+                    break;
+                }
+                // the block's MMAs are complete and its scales read
+                __syncwarp();
+                if (lane == 0)
+                    mbar_arrive(empty_bar + 8 * stage);
+                tc_fence_after();
+                uint32_t r[SK_TOK];
+                tmem_ld_chunk(tmem_base + ((uint32_t)(quarter * 32) << 16) + buf * (2 * SK_TOK) + half * SK_TOK, r);
+                tmem_wait_ld_chunk(r);
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0)
+                    mbar_arrive(tempty_bar + 8 * stage);
+#pragma unroll
+                for (int j = 0; j < SK_TOK / 2; ++j)
+                    acc[j] = __ffma2_rn(make_float2(__uint_as_float(r[2 * j]), __uint_as_float(r[2 * j + 1])), sc[j],
+                                        acc[j]);
+                if (++buf == NB) {
+                    buf = 0;
+                    tphase ^= 1;
+                }
+                if (++stage == NS) {
+                    stage = 0;
+                    phase ^= 1;
+                }
+            }
+            if (!ok || !half_ok)
+                continue;
+#pragma unroll
+            for (int j = 0; j < SK_TOK; ++j) {
+                if (j < nrows) {
+                    const float v = (j & 1) ? acc[j >> 1].y : acc[j >> 1].x;
+                    const int64_t at = (tl.m0 + j) * p.ldc + n;
+                    if constexpr (OUT == OUT_BF16)
+                        static_cast<__nv_bfloat16 *>(p.C)[at] = __float2bfloat16_rn(v);
+                    else
+                        static_cast<float *>(p.C)[at] = v;
+                }
+            }
+        }
+    }
 }
 
 template <int MODE, int OUT>
@@ -288,7 +596,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         tma_prefetch_desc(&tmB);
         if constexpr (!gathered)
             tma_prefetch_desc(&tmSA);
-        if constexpr (MODE == WGRAD)
+        if constexpr (MODE == WGRAD || MODE == GROUPED_C)
             tma_prefetch_desc(&tmSB);
     }
     if (warp == 1) {
@@ -300,26 +608,66 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     // quantiser, which lets this grid launch under its last wave) are read
     // only after this wait.
     griddep_wait();
-    if constexpr (is_grouped(MODE))
-        build_group_prefix<NUM_THREADS>(p.expert_offsets, p.n_experts, p.n_rows, p.num_n_tiles, BM, p.status, prefix,
-                                        reinterpret_cast<int32_t *>(smem + L::stage_c_off));
+    // This CTA's tiles: t = cta, cta + ncta, ... below num_tiles. With
+    // skinny tiles the first `s` CTAs take the skinny experts and the rest
+    // the others (every CTA derives the same split from the offsets).
+    int64_t num_tiles = p.num_m_tiles * p.num_n_tiles;
+    int cta = (int)blockIdx.x, ncta = (int)gridDim.x;
+    bool skinny = false;
+    if constexpr (is_grouped(MODE)) {
+        int32_t *scan = reinterpret_cast<int32_t *>(smem + L::stage_c_off);
+        if (MODE == GROUPED_C && p.skinny_rows > 0) {
+            build_group_prefix<NUM_THREADS>(p.expert_offsets, p.n_experts, p.n_rows, p.num_n_tiles, BM, p.status,
+                                            prefix, scan, p.skinny_rows, ROWS_UP_TO);
+            const int64_t skinny_tiles = prefix[p.n_experts];
+            build_group_prefix<NUM_THREADS>(p.expert_offsets, p.n_experts, p.n_rows, p.num_n_tiles, BM, p.status,
+                                            prefix, scan, p.skinny_rows, ROWS_ABOVE);
+            const int64_t full_tiles = prefix[p.n_experts];
+            const int s = skinny_cta_count(full_tiles, skinny_tiles, (int)gridDim.x, p.skinny_cost_pct);
+            if ((int)blockIdx.x < s) {
+                skinny = true;
+                ncta = s;
+                num_tiles = skinny_tiles;
+                build_group_prefix<NUM_THREADS>(p.expert_offsets, p.n_experts, p.n_rows, p.num_n_tiles, BM,
+                                                p.status, prefix, scan, p.skinny_rows, ROWS_UP_TO);
+                // (after the last pass has read its scratch, which these
+                // barriers overwrite)
+                if (threadIdx.x == 0)
+                    skinny_init_barriers(sbase);
+            } else {
+                cta = (int)blockIdx.x - s;
+                ncta = (int)gridDim.x - s;
+                num_tiles = full_tiles;
+            }
+        } else {
+            build_group_prefix<NUM_THREADS>(p.expert_offsets, p.n_experts, p.n_rows, p.num_n_tiles, BM, p.status,
+                                            prefix, scan);
+            num_tiles = prefix[p.n_experts];
+        }
+    }
+    volatile Sched *sched = reinterpret_cast<volatile Sched *>(smem + L::sched_off);
+    if (threadIdx.x == 0) {
+        sched->count = num_tiles;
+        sched->first = cta;
+        sched->stride = ncta;
+    }
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem_base = *tmem_ptr;
-
-    const int64_t num_tiles =
-        is_grouped(MODE) ? (int64_t)prefix[p.n_experts] : p.num_m_tiles * p.num_n_tiles;
     const int num_kb = (int)(p.K / BK);
 
-    if (warp == 0) {
+    if (MODE == GROUPED_C && skinny) {
+        if constexpr (MODE == GROUPED_C)
+            skinny_roles<OUT>(&tmSB, &tmB, &tmSA, p, smem, prefix, sched, tmem_base, wc, warp, lane);
+    } else if (warp == 0) {
         // ------------------------------------------------------ producer ----
         setmaxnreg_dec<Regs<MODE>::LOW>();
         uint32_t stage = 0, phase = 0;
         uint32_t filled_mask = 0, fill_parity = 0;  // per stage: a fill was issued, and its parity
         bool skip = p.skip_first_load && blockIdx.x == 0;
         bool ok = true;
-        for (int64_t t = blockIdx.x; t < num_tiles && ok; t += gridDim.x) {
+        for (int64_t t = sched->first; t < sched->count && ok; t += sched->stride) {
             const Tile tl = decode_tile<MODE>(t, p, prefix);
             for (int kb = 0; kb < num_kb; ++kb) {
                 bool got = true;
@@ -426,7 +774,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             uint32_t last_buf = 0, last_par = 0;
             bool ok = true;
             int64_t g = 0;  // the CTA's block counter (tile-major)
-            for (int64_t t = blockIdx.x; t < num_tiles && ok; t += gridDim.x) {
+            for (int64_t t = sched->first; t < sched->count && ok; t += sched->stride) {
                 for (int kb = 0; kb < num_kb; ++kb, ++g) {
                     if ((int)(g % NI) != issuer)
                         continue;
@@ -499,7 +847,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         uint32_t buf = 0, tphase = 0;        // TMEM partial buffer
         uint32_t stage = 0, phase = 0;       // pipeline stage holding the block's scales
         bool ok = true;
-        for (int64_t t = blockIdx.x; t < num_tiles && ok; t += gridDim.x) {
+        for (int64_t t = sched->first; t < sched->count && ok; t += sched->stride) {
             const Tile tl = decode_tile<MODE>(t, p, prefix);
             const int64_t row = tl.m0 + row_in_tile;  // A row (dense) / output row (grouped)
             const bool row_ok = row < tl.row_end;
@@ -718,7 +1066,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             arrive_stage = arrive_stage + 1 == STAGES ? 0 : arrive_stage + 1;
             ++arrived;
         };
-        for (int64_t t = blockIdx.x; t < num_tiles && ok; t += gridDim.x) {
+        for (int64_t t = sched->first; t < sched->count && ok; t += sched->stride) {
             const Tile tl = decode_tile<MODE>(t, p, prefix);
             const int64_t left = tl.row_end - tl.m0;
             const int nvalid = left < BM ? (int)left : BM;  // valid rows of the tile
@@ -1057,8 +1405,17 @@ extern "C" int fp8_grouped_gemm(const uint8_t *Xq, const float *sX, int64_t ld_s
         return FP8FG_ECUDA;
     if (!make_map_f32_row(&m.sa, sX, (uint64_t)n_tokens, (uint64_t)(K / BK), (uint64_t)ld_sX, SA_BOX))
         return FP8FG_ECUDA;
-    m.sb = m.sa;  // unused
     const int grid = sm_count();
+    if (row_index) {
+        m.sb = m.sa;  // unused
+    } else {
+        // the skinny tiles' token rows: 32-row boxes (the fourth map, which
+        // carries column scales only for the weight gradient)
+        if (!make_map(&m.sb, Xq, (uint64_t)K, (uint64_t)n_tokens, (uint64_t)K, BK, SK_TOK))
+            return FP8FG_ECUDA;
+        p.skinny_rows = grid >= 2 ? grouped_skinny_rows() : 0;
+        p.skinny_cost_pct = grouped_skinny_cost_pct();
+    }
     if (row_index)
         return launch_out<GROUPED>(out, m, p, grid > 0 ? grid : 1, static_cast<cudaStream_t>(stream));
     return launch_out<GROUPED_C>(out, m, p, grid > 0 ? grid : 1, static_cast<cudaStream_t>(stream));

@@ -18,15 +18,22 @@ struct GroupTile {
     int expert;
 };
 
+// Which experts a prefix counts: those with more than `small` rows
+// (small = 0: every non-empty expert), or the non-empty ones with at most
+// `small` rows.
+enum GroupSet { ROWS_ABOVE = 0, ROWS_UP_TO = 1 };
+
 // Block-wide exclusive prefix over experts of (m-tiles x n-tiles) into
-// prefix[0..E] (prefix[E] = total tiles); malformed offsets are reported as
-// FP8FG_EDEVICE and clamped. All NT threads of the block call it;
-// warp_sums is NT/32 ints of shared scratch (the kernels lend a region
-// that is idle during their prologue, so they declare no static shared
-// memory that would push their aligned dynamic region).
+// prefix[0..E] (prefix[E] = total tiles), counting only the experts of
+// `which`; malformed offsets are reported as FP8FG_EDEVICE and clamped. All
+// NT threads of the block call it; warp_sums is NT/32 ints of shared
+// scratch (the kernels lend a region that is idle during their prologue, so
+// they declare no static shared memory that would push their aligned
+// dynamic region).
 template <int NT>
 __device__ void build_group_prefix(const int32_t *offsets, int E, int64_t n_rows, int64_t n_tiles_n, int bm,
-                                   int *status, int32_t *prefix, int32_t *warp_sums)
+                                   int *status, int32_t *prefix, int32_t *warp_sums, int64_t small = 0,
+                                   GroupSet which = ROWS_ABOVE)
 {
     const int per = (E + NT - 1) / NT;
     const int e0 = threadIdx.x * per;
@@ -42,7 +49,8 @@ __device__ void build_group_prefix(const int32_t *offsets, int E, int64_t n_rows
             r0 = r0 < 0 ? 0 : (r0 > n_rows ? n_rows : r0);
             r1 = r1 > n_rows ? n_rows : r1;
             const int64_t m = r1 > r0 ? r1 - r0 : 0;
-            v = (int32_t)(((m + bm - 1) / bm) * n_tiles_n);
+            if (which == ROWS_ABOVE ? m > small : m <= small)
+                v = (int32_t)(((m + bm - 1) / bm) * n_tiles_n);
         }
         local[i] = v;
         sum += v;

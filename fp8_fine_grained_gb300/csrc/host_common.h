@@ -22,6 +22,12 @@ uint64_t wait_limit_ns();
 // One-shot test hook consumed by the next GEMM launch on the current device.
 bool take_skip_first_load();
 
+// Schedule of the grouped GEMM with rows in expert order: the skinny-tile
+// row threshold (0: off) and a skinny tile's SM time relative to a full
+// tile, in percent.
+int grouped_skinny_rows();
+int grouped_skinny_cost_pct();
+
 // Current device is a Blackwell sm_103 part (cached per device).
 bool device_supported();
 

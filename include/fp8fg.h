@@ -320,6 +320,12 @@ FP8FG_API int fp8_gemm_blockscaled_e4m3(int mode,
  *   below 2^31 (else EINVAL).
  *   Alignment: Xq, Wq, sX, Y 16-byte aligned; K % 16 == 0; ld_sX % 4 == 0;
  *   ldy*sizeof(out) % 16 == 0.
+ *   Tiles: 128 rows of an expert x 256 columns. With row_index == NULL,
+ *   experts with at most 32 rows (fp8fg_set_grouped_schedule) are computed
+ *   instead as 256 weight rows x their (up to) 32 token rows per tile, with
+ *   the weight as the tensor cores' 128-row operand; the sum and its
+ *   promotion per 128-wide contraction block are the same. Part of the SMs
+ *   takes those tiles while the others take the rest.
  * ------------------------------------------------------------------- */
 FP8FG_API int fp8_grouped_gemm(const uint8_t *Xq, const float *sX, int64_t ld_sX, int64_t n_tokens,
                      const int32_t *row_index, const int32_t *expert_offsets,
@@ -465,6 +471,16 @@ FP8FG_API int fp8fg_test_skip_first_load(int skip);
 /* Wait limit of the device-side bounded waits, in nanoseconds (default two
  * seconds). Values below 1e6 are raised to 1e6. Returns FP8FG_OK. */
 FP8FG_API int fp8fg_set_wait_limit_ns(int64_t ns);
+
+/* Schedule of fp8_grouped_gemm with rows in expert order (row_index ==
+ * NULL); results do not depend on it. Experts with at most `skinny_rows`
+ * rows take skinny tiles (0 turns them off; default 32, at most 32), and
+ * `skinny_cost_pct` is the SM time of one skinny tile relative to a full
+ * tile, in percent (default 100), which sets the share of the SMs the
+ * skinny tiles get. Process-wide; read at each launch. Returns FP8FG_OK,
+ * or FP8FG_EINVAL (nothing changed) unless 0 <= skinny_rows <= 32 and
+ * 1 <= skinny_cost_pct <= 1000. */
+FP8FG_API int fp8fg_set_grouped_schedule(int skinny_rows, int skinny_cost_pct);
 
 #ifdef __cplusplus
 }

@@ -320,3 +320,18 @@ def test_moe_combine_validation(L):
     assert call(T=0) == 0
     assert call(N=0, ldy=0, ldo=0) == 0
     assert call() in (EUNSUPPORTED, 4)
+
+
+def test_grouped_schedule_validation(L):
+    f = L.fp8fg_set_grouped_schedule
+    assert f(-1, 100) == EINVAL
+    assert f(33, 100) == EINVAL                      # skinny tiles hold 32 token rows
+    assert f(32, 0) == EINVAL
+    assert f(32, 1001) == EINVAL
+    try:
+        assert f(0, 1) == 0
+        assert f(16, 1000) == 0
+        with pytest.raises(fg.Fp8fgError):
+            fg.set_grouped_schedule(40)
+    finally:
+        assert f(32, 100) == 0                       # the defaults
