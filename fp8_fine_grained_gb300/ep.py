@@ -37,7 +37,9 @@ One layer, per rank:
 
 On one rank (world 1, moe_forward with pg=None) steps 3 and 5's reorder
 are identities: the send buffer is the expert GEMM's input, in expert
-order, and the combine reads the GEMM's output directly.
+order (the GEMM's form without a row index, which runs experts of at most
+32 rows as skinny tiles), and the combine reads the GEMM's output
+directly.
 
 What runs where: steps 1, 4 and 5's reorder are index bookkeeping and row
 moves in torch (no FP8 arithmetic), the exchanges are collectives, every
